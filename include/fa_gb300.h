@@ -1,0 +1,154 @@
+/*
+ * fa_gb300.h -- C ABI of the GB300 (sm_103a) variable-length attention
+ * forward library (libfa_gb300.so).
+ *
+ * The library computes, for packed variable-length sequences,
+ *
+ *     O = softmax(scale * Q Kᵀ + mask) V        (online softmax, fp32 state)
+ *     LSE = log-sum-exp of the masked, scaled scores (natural log)
+ *
+ * and the sparse-MLA decode variant that attends over per-token top-k rows
+ * gathered from a paged 576-wide latent cache.
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are caller-owned device buffers, C-contiguous, 16-byte
+ *     aligned.  bf16 means IEEE bfloat16 bit patterns (2 bytes).
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream).  The
+ *     library allocates no memory, performs no host<->device copy and never
+ *     synchronises; it only encodes TMA descriptors on the host and launches.
+ *     The first call on a device queries device attributes once; make it
+ *     before any stream capture that is to contain a call.
+ *   - Errors detected on the host (argument checks) are returned before any
+ *     launch and leave every output untouched.  A launch failure returns
+ *     FA_ERR_LAUNCH.  Problems found on the device (a pipeline wait that ran
+ *     out of time) set a device status word that fa_get_device_status()
+ *     reports; outputs of that call are then undefined.
+ *   - Results are bitwise deterministic run to run for identical inputs.
+ *
+ * Sources of the semantics (web pages the interface is taken from):
+ *   [flash_attn]   vLLM API docs, "vllm.v1.attention.backends.mla.prefill.
+ *                  flash_attn": FA4MLAPrefillKernel (CompileKey fields: q/k/v
+ *                  shapes, cu_seqlens, max_seqlen, softmax_scale, causal,
+ *                  window_size, return_softmax_lse), FlashAttnPrefillBackend
+ *                  (run_prefill_new_tokens: causal, cu_seqlens_q ==
+ *                  cu_seqlens_k; run_prefill_context_chunk: non-causal,
+ *                  returns the LSE), FA4SplitKVCombineKernel (LSE laid out
+ *                  [num_heads, total_q]).
+ *   [sglang-fa4]   sglang PR #41344, "fill gaps in FA4 path on Blackwell":
+ *                  "Motivation" and "Modifications" (row max, exp2, rescale
+ *                  threshold, masking only boundary tiles), "Accuracy Tests"
+ *                  (chunked prefill with q shorter than k; head dims
+ *                  64/96/128/(192,128); sliding window), "Speed Tests and
+ *                  Profiling" (ViT head dims 64/72/80/128).
+ *   [mla_sparse]   vLLM API docs, "vllm.v1.attention.backends.mla.
+ *                  flashattn_mla_sparse": FlashAttnMLASparseFA4Backend (BF16
+ *                  cache only, head size 576 = 512 latent + 64 rope, block
+ *                  size a multiple of 64, index_topk % 128 == 0, 8..128
+ *                  query heads) and _fa4_varlen_scalars (one query row per
+ *                  token).
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers. */
+typedef struct CUstream_st* fa_stream_t;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned buffer */
+  FA_ERR_UNSUPPORTED = 2,   /* valid request outside what is compiled in */
+  FA_ERR_ARCH = 3,          /* current device is not sm_103 (GB300) */
+  FA_ERR_LAUNCH = 4,        /* CUDA launch or driver call failed */
+  FA_ERR_DEVICE_TIMEOUT = 5 /* reported by fa_get_device_status only */
+} fa_status;
+
+/*
+ * fa_varlen_fwd -- attention forward over packed variable-length sequences.
+ * Defined by [flash_attn] (flash_attn_varlen_func keyword arguments as used
+ * by run_prefill_new_tokens / run_prefill_context_chunk) and [sglang-fa4].
+ *
+ *   q             bf16 [total_q, num_heads,   d_qk]
+ *   k             bf16 [total_k, num_heads_k, d_qk]
+ *   v             bf16 [total_k, num_heads_k, d_v]
+ *   cu_seqlens_q  int32 [batch + 1] device, non-decreasing, cu[0] = 0,
+ *                 cu[batch] = total_q.  Sequence b owns query tokens
+ *                 [cu_seqlens_q[b], cu_seqlens_q[b+1]).
+ *   cu_seqlens_k  int32 [batch + 1] device, same for keys/values.
+ *   batch         1 .. 1024
+ *   num_heads, num_heads_k  num_heads % num_heads_k == 0; query head h reads
+ *                 key/value head h / (num_heads / num_heads_k).
+ *   (d_qk, d_v)   one of (64,64) (72,72) (80,80) (96,96) (128,128) (192,128).
+ *   max_seqlen_q, max_seqlen_k  host hints only (never used for
+ *                 correctness; may be 0).
+ *   softmax_scale scale applied to Q Kᵀ before the softmax (> 0).
+ *   causal        nonzero: key j is visible to query row i of a sequence iff
+ *                 j <= i + (Lk - Lq), i.e. the diagonal is aligned to the
+ *                 bottom-right corner (chunked prefill with Lq < Lk).
+ *   window_left, window_right  sliding window, inclusive, in the same
+ *                 bottom-right frame: j >= i + (Lk-Lq) - window_left and
+ *                 j <= i + (Lk-Lq) + window_right; -1 = unbounded.
+ *   out           bf16 [total_q, num_heads, d_v]  (written)
+ *   lse           fp32 [num_heads, total_q] natural-log LSE, or NULL.
+ *
+ * A query row with no visible key gets O = 0 and LSE = -inf.
+ * Host errors: FA_ERR_INVALID_ARG (null required pointer, negative sizes,
+ * batch < 1, head counts, window < -1, scale <= 0, unaligned pointers),
+ * FA_ERR_UNSUPPORTED (head dims, batch > 1024), FA_ERR_ARCH.
+ */
+fa_status fa_varlen_fwd(const void* q, const void* k, const void* v,
+                        const int* cu_seqlens_q, const int* cu_seqlens_k,
+                        int batch, int total_q, int total_k, int num_heads,
+                        int num_heads_k, int d_qk, int d_v, int max_seqlen_q,
+                        int max_seqlen_k, float softmax_scale, int causal,
+                        int window_left, int window_right, void* out,
+                        float* lse, fa_stream_t stream);
+
+/*
+ * fa_sparse_mla_decode -- one query row per token attending over top-k rows
+ * gathered from a paged latent cache shared by all heads.  Defined by
+ * [mla_sparse] (FlashAttnMLASparseFA4Backend, _fa4_varlen_scalars).
+ *
+ *   q             bf16 [num_tokens, num_heads, 576]
+ *   kv_cache      bf16 [num_pages, 64, 576]: 512 latent + 64 rope columns
+ *   page_table    int32 [num_tokens, max_pages_per_tok]: physical page of
+ *                 each logical page of the token's context
+ *   topk_idx      int32 [num_tokens, topk]: logical positions p in the
+ *                 token's context; row = page_table[t, p/64]*64 + p%64.
+ *                 A slot with p < 0, p >= 64*max_pages_per_tok or a page id
+ *                 outside [0, num_pages) is skipped (contributes nothing).
+ *   num_heads     one of 8, 16, 32, 64, 128
+ *   topk          multiple of 128, 128 .. 64*max_pages_per_tok
+ *   softmax_scale scale of the 576-wide dot product (> 0)
+ *   out           bf16 [num_tokens, num_heads, 512]: sum_j p_j * row_j[0:512]
+ *   lse           fp32 [num_heads, num_tokens] or NULL
+ *
+ * Host errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (heads, topk),
+ * FA_ERR_ARCH.
+ */
+fa_status fa_sparse_mla_decode(const void* q, const void* kv_cache,
+                               const int* page_table, const int* topk_idx,
+                               int num_tokens, int num_heads, int topk,
+                               int num_pages, int max_pages_per_tok,
+                               float softmax_scale, void* out, float* lse,
+                               fa_stream_t stream);
+
+/*
+ * fa_get_device_status -- reads and clears the library's device status word
+ * on the current device.  Synchronises the device (not for the hot path).
+ * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT if a kernel abandoned a pipeline wait
+ * since the last call, or FA_ERR_LAUNCH if the read itself failed.
+ */
+fa_status fa_get_device_status(void);
+
+/* Human-readable name of a status code (static string). */
+const char* fa_status_string(fa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,114 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function the header declares, and rejects bad arguments on the host before
+touching CUDA."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import varlen_flashattention_forward_gb300 as fa
+from varlen_flashattention_forward_gb300 import build_ext
+
+REPO = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(REPO, "include", "fa_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_ext.build()
+    return fa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:fa_status|const char\*)\s+(fa_\w+)\s*\(", text,
+                                 flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    assert declared_functions() == sorted(fa.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", build_ext.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(\w+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.fa_status_string(s)
+    assert lib.fa_status_string(2).decode() == "unsupported configuration"
+
+
+P = ctypes.c_void_p
+
+
+def varlen(lib, **kw):
+    a = dict(q=P(0x1000), k=P(0x2000), v=P(0x3000), cq=P(0x4000), ck=P(0x5000), batch=2,
+             total_q=10, total_k=10, H=4, Hk=4, dqk=64, dv=64, mq=5, mk=5, scale=0.125,
+             causal=0, wl=-1, wr=-1, out=P(0x6000), lse=None, stream=None)
+    a.update(kw)
+    return lib.fa_varlen_fwd(a["q"], a["k"], a["v"], a["cq"], a["ck"], a["batch"], a["total_q"],
+                             a["total_k"], a["H"], a["Hk"], a["dqk"], a["dv"], a["mq"], a["mk"],
+                             a["scale"], a["causal"], a["wl"], a["wr"], a["out"], a["lse"],
+                             a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(out=None), fa.FA_ERR_INVALID_ARG),
+    (dict(cq=None), fa.FA_ERR_INVALID_ARG),
+    (dict(k=None), fa.FA_ERR_INVALID_ARG),
+    (dict(batch=0), fa.FA_ERR_INVALID_ARG),
+    (dict(total_q=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(H=6, Hk=4), fa.FA_ERR_INVALID_ARG),
+    (dict(Hk=0), fa.FA_ERR_INVALID_ARG),
+    (dict(wl=-2), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(q=P(0x1008)), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=P(0x6002)), fa.FA_ERR_INVALID_ARG),
+    (dict(dqk=100, dv=100), fa.FA_ERR_UNSUPPORTED),
+    (dict(dqk=192, dv=192), fa.FA_ERR_UNSUPPORTED),
+    (dict(batch=1025), fa.FA_ERR_UNSUPPORTED),
+])
+def test_varlen_host_validation(lib, kw, expect):
+    assert varlen(lib, **kw) == expect
+
+
+def decode(lib, **kw):
+    a = dict(q=P(0x1000), c=P(0x2000), pt=P(0x3000), ti=P(0x4000), T=4, H=64, topk=256,
+             pages=100, maxp=16, scale=0.04, out=P(0x5000), lse=None, stream=None)
+    a.update(kw)
+    return lib.fa_sparse_mla_decode(a["q"], a["c"], a["pt"], a["ti"], a["T"], a["H"], a["topk"],
+                                    a["pages"], a["maxp"], a["scale"], a["out"], a["lse"],
+                                    a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(ti=None), fa.FA_ERR_INVALID_ARG),
+    (dict(T=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(c=P(0x2004)), fa.FA_ERR_INVALID_ARG),
+    (dict(H=48), fa.FA_ERR_UNSUPPORTED),
+    (dict(topk=200), fa.FA_ERR_UNSUPPORTED),
+    (dict(topk=2048, maxp=16), fa.FA_ERR_UNSUPPORTED),
+])
+def test_decode_host_validation(lib, kw, expect):
+    assert decode(lib, **kw) == expect
+
+
+def test_valid_arguments_without_gpu_fail_cleanly(lib):
+    """With no usable device the call returns a status instead of crashing."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert varlen(lib) in (fa.FA_ERR_LAUNCH, fa.FA_ERR_ARCH)

@@ -1,0 +1,178 @@
+"""GPU parity of fa_varlen_fwd (through the C ABI) against the fp64 oracle.
+
+Tolerances: max |O_gpu - O_oracle| <= 2e-2 on the bf16 output and
+max |LSE_gpu - LSE_oracle| <= 1e-3 on the fp32 LSE, element by element on
+small cases that still span several tiles and a ragged tail, and on sampled
+rows at the full workload sizes.  Results must be bitwise identical run to
+run.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import varlen_flashattention_forward_gb300 as fa
+from varlen_flashattention_forward_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 2e-2
+LSE_TOL = 1e-3
+
+
+def cu(lens):
+    c = [0]
+    for L in lens:
+        c.append(c[-1] + L)
+    return torch.tensor(c, dtype=torch.int32)
+
+
+def make(lens_q, lens_k, H, Hk, dqk, dv, seed, std=1.0):
+    g = torch.Generator().manual_seed(seed)
+    q = (torch.randn(sum(lens_q), H, dqk, generator=g) * std).bfloat16()
+    k = (torch.randn(sum(lens_k), Hk, dqk, generator=g) * std).bfloat16()
+    v = torch.randn(sum(lens_k), Hk, dv, generator=g).bfloat16()
+    return q, k, v, cu(lens_q), cu(lens_k)
+
+
+def run_gpu(q, k, v, cq, ck, scale, causal=False, wl=-1, wr=-1):
+    dev = torch.device("cuda:0")
+    out, lse = fa.fa_varlen_fwd(q.to(dev), k.to(dev), v.to(dev), cq.to(dev), ck.to(dev),
+                                0, 0, scale, causal, wl, wr, return_lse=True)
+    torch.cuda.synchronize()
+    return out.cpu(), lse.cpu()
+
+
+def compare(q, k, v, cq, ck, scale, causal=False, wl=-1, wr=-1, rows=None, out=None, lse=None):
+    if out is None:
+        out, lse = run_gpu(q, k, v, cq, ck, scale, causal, wl, wr)
+    ref_o, ref_l = oracle.varlen_attention(q, k, v, cq, ck, scale, causal, wl, wr, rows=rows)
+    T, H, dv = out.shape
+    go = out.float().numpy().reshape(T * H, dv)
+    gl = lse.numpy().T.reshape(T * H)
+    if rows is not None:
+        go, gl = go[rows], gl[rows]
+    err_o = np.abs(go - ref_o).max() if go.size else 0.0
+    fin = np.isfinite(ref_l)
+    assert np.array_equal(np.isfinite(gl), fin), "LSE -inf pattern differs"
+    assert np.all(gl[~fin] == -np.inf)
+    err_l = np.abs(gl[fin] - ref_l[fin]).max() if fin.any() else 0.0
+    assert err_o <= O_TOL, f"max|dO| = {err_o}"
+    assert err_l <= LSE_TOL, f"max|dLSE| = {err_l}"
+    return err_o, err_l
+
+
+RAGGED = [1, 63, 64, 127, 128, 129, 255, 257, 300, 513]
+
+
+def test_status_word_starts_clear(cuda_device):
+    assert fa.fa_get_device_status() == fa.FA_OK
+
+
+def test_tiny_workload_elementwise(cuda_device):
+    w = workloads.tiny()
+    q, k, v, cq, ck = w.make_inputs()
+    compare(q, k, v, cq, ck, w.softmax_scale)
+
+
+@pytest.mark.parametrize("dqk,dv", [(64, 64), (72, 72), (80, 80), (96, 96), (128, 128), (192, 128)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dims_ragged_elementwise(cuda_device, dqk, dv, causal):
+    q, k, v, cq, ck = make(RAGGED, RAGGED, 2, 2, dqk, dv, seed=dqk + dv + causal)
+    compare(q, k, v, cq, ck, dqk ** -0.5, causal)
+
+
+def test_chunked_prefill_bottom_right(cuda_device):
+    lens_q, lens_k = [5, 130, 256, 1, 200], [300, 400, 1000, 129, 200]
+    q, k, v, cq, ck = make(lens_q, lens_k, 3, 3, 192, 128, seed=7)
+    compare(q, k, v, cq, ck, 192 ** -0.5, causal=True)
+
+
+def test_q_longer_than_k_has_empty_rows(cuda_device):
+    lens_q, lens_k = [300, 40, 128], [100, 0, 1]
+    q, k, v, cq, ck = make(lens_q, lens_k, 2, 2, 64, 64, seed=8)
+    compare(q, k, v, cq, ck, 0.125, causal=True)
+    compare(q, k, v, cq, ck, 0.125, causal=False)
+
+
+def test_zero_length_sequences(cuda_device):
+    lens_q, lens_k = [0, 17, 0, 140, 0], [0, 17, 5, 140, 0]
+    q, k, v, cq, ck = make(lens_q, lens_k, 2, 2, 80, 80, seed=9)
+    compare(q, k, v, cq, ck, 80 ** -0.5)
+
+
+@pytest.mark.parametrize("wl,wr,causal", [(1024, 0, True), (100, 0, True), (127, 0, True),
+                                          (128, 0, True), (50, 70, False), (0, 0, False),
+                                          (-1, 5, False), (300, -1, False)])
+def test_sliding_windows(cuda_device, wl, wr, causal):
+    lens = [1500, 257, 64, 700]
+    q, k, v, cq, ck = make(lens, lens, 2, 2, 128, 128, seed=10 + wl + wr)
+    compare(q, k, v, cq, ck, 128 ** -0.5, causal, wl, wr)
+
+
+def test_gqa(cuda_device):
+    lens = [300, 77]
+    q, k, v, cq, ck = make(lens, lens, 8, 2, 128, 128, seed=11)
+    compare(q, k, v, cq, ck, 128 ** -0.5, causal=True)
+
+
+def test_large_scores_need_rescale(cuda_device):
+    """Score ranges far beyond the lazy-rescale threshold, growing along the
+    key axis so the running max moves many times."""
+    lens = [1000, 600]
+    q, k, v, cq, ck = make(lens, lens, 2, 2, 64, 64, seed=12, std=3.0)
+    ramp = torch.linspace(0.2, 3.0, k.shape[0])[:, None, None]
+    k = (k.float() * ramp).bfloat16()
+    compare(q, k, v, cq, ck, 0.5)
+    compare(q, k, v, cq, ck, 0.5, causal=True)
+
+
+def test_single_key_returns_v_exactly(cuda_device):
+    lens = [1, 1, 1, 1]
+    q, k, v, cq, ck = make(lens, lens, 4, 4, 64, 64, seed=13)
+    out, lse = run_gpu(q, k, v, cq, ck, 0.125)
+    assert torch.equal(out, v)
+
+
+def test_bitwise_deterministic(cuda_device):
+    w = workloads.tiny()
+    lens = [3000, 50, 1200]
+    q, k, v, cq, ck = make(lens, lens, 4, 4, 80, 80, seed=14)
+    a = run_gpu(q, k, v, cq, ck, 80 ** -0.5, causal=True)
+    b = run_gpu(q, k, v, cq, ck, 80 ** -0.5, causal=True)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_max_batch(cuda_device):
+    lens = [(i * 37) % 130 for i in range(1024)]
+    q, k, v, cq, ck = make(lens, lens, 1, 1, 64, 64, seed=15)
+    compare(q, k, v, cq, ck, 0.125)
+
+
+# ------------------------------------------------------------ full sizes
+def sample_rows(lens_q, H, n, seed):
+    """Boundary rows of every sequence plus random rows, all as token*H+head."""
+    rng = np.random.default_rng(seed)
+    toks = []
+    s = 0
+    for L in lens_q:
+        if L:
+            toks += [s, s + L - 1, s + min(L - 1, 127), s + min(L - 1, 128)]
+        s += L
+    toks = np.array(toks + list(rng.integers(0, s, size=n)), dtype=np.int64)
+    heads = rng.integers(0, H, size=toks.shape[0])
+    return np.unique(toks * H + heads)
+
+
+FULL = ["vit_full_d80", "vit_full_d64", "vit_full_d72", "vit_full_d128", "vit_window_d80",
+        "long_16384", "long_65536", "mla_causal", "mla_chunked", "mla_swa"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_rows(cuda_device, name):
+    w = workloads.VARLEN_BENCH[name]()
+    q, k, v, cq, ck = w.make_inputs()
+    out, lse = run_gpu(q, k, v, cq, ck, w.softmax_scale, w.causal, *w.window)
+    rows = sample_rows(w.lens_q, w.num_heads, 160, seed=len(name))
+    compare(q, k, v, cq, ck, w.softmax_scale, w.causal, *w.window, rows=rows, out=out, lse=lse)
+    assert fa.fa_get_device_status() == fa.FA_OK

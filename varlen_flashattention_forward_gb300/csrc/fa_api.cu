@@ -1,0 +1,263 @@
+// fa_api.cu -- host side of the C ABI declared in include/fa_gb300.h:
+// argument validation, TMA descriptor encoding, dispatch over the compiled
+// head-dim instantiations, and the device status word.
+//
+// No function here allocates device memory, copies data or synchronises,
+// except fa_get_device_status (documented as synchronising).
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fa_gb300.h"
+#include "sparse_decode_kernel.cuh"
+#include "varlen_fwd_kernel.cuh"
+
+namespace fa {
+cudaError_t launch_varlen_64_64(const VarlenMaps&, const VarlenArgs&, int, cudaStream_t);
+cudaError_t launch_varlen_72_72(const VarlenMaps&, const VarlenArgs&, int, cudaStream_t);
+cudaError_t launch_varlen_80_80(const VarlenMaps&, const VarlenArgs&, int, cudaStream_t);
+cudaError_t launch_varlen_96_96(const VarlenMaps&, const VarlenArgs&, int, cudaStream_t);
+cudaError_t launch_varlen_128_128(const VarlenMaps&, const VarlenArgs&, int, cudaStream_t);
+cudaError_t launch_varlen_192_128(const VarlenMaps&, const VarlenArgs&, int, cudaStream_t);
+}  // namespace fa
+
+// Device status word: bit 0 = a pipeline wait ran out of time.
+__device__ unsigned int g_fa_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  bool arch_ok = false;
+  int sm_count = 0;
+  unsigned int* status = nullptr;  // device address of g_fa_status
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Per-device facts, queried once.  The first call on a device therefore
+// performs runtime queries (no stream work); make it before any stream
+// capture if the call is to be captured.
+fa_status device_info(DeviceInfo** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FA_ERR_LAUNCH;
+    d.arch_ok = (major == 10 && minor == 3);
+    d.sm_count = sms;
+    void* p = nullptr;
+    if (d.arch_ok) {
+      if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) return FA_ERR_LAUNCH;
+    }
+    d.status = static_cast<unsigned int*>(p);
+    d.ready = true;
+  }
+  *out = &d;
+  return d.arch_ok ? FA_OK : FA_ERR_ARCH;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D bf16 tensor [tokens, heads, dim] (dim innermost) viewed through a box of
+// {box_w, 1, box_rows}.  The swizzle matches the box width (64 -> 128 B,
+// 32 -> 64 B, 16 -> 32 B).  Elements past `dim` or `tokens` read as zero.
+bool encode_rows(CUtensorMap* m, const void* base, int dim, int heads, int tokens, int box_w,
+                 int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)dim, (cuuint64_t)heads,
+                        (cuuint64_t)(tokens > 0 ? tokens : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)dim * 2, (cuuint64_t)heads * dim * 2};
+  cuuint32_t box[3] = {(cuuint32_t)box_w, 1u, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUtensorMapSwizzle swz = box_w == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                           : box_w == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                         : CU_TENSOR_MAP_SWIZZLE_32B;
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int tail_width(int d) { return ((d + 15) / 16 * 16) % 64; }
+
+}  // namespace
+
+extern "C" fa_status fa_varlen_fwd(const void* q, const void* k, const void* v,
+                                   const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                                   int total_q, int total_k, int num_heads, int num_heads_k,
+                                   int d_qk, int d_v, int max_seqlen_q, int max_seqlen_k,
+                                   float softmax_scale, int causal, int window_left,
+                                   int window_right, void* out, float* lse,
+                                   fa_stream_t stream) {
+  (void)max_seqlen_q;
+  (void)max_seqlen_k;
+  // ---- host validation (before any CUDA call)
+  if (!q || !out || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
+  if (total_k > 0 && (!k || !v)) return FA_ERR_INVALID_ARG;
+  if (batch < 1 || total_q < 0 || total_k < 0 || num_heads < 1 || num_heads_k < 1 ||
+      num_heads % num_heads_k != 0)
+    return FA_ERR_INVALID_ARG;
+  if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || (k && !aligned(k, 16)) || (v && !aligned(v, 16)) ||
+      !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4) || (lse && !aligned(lse, 4)))
+    return FA_ERR_INVALID_ARG;
+  if (batch > fa::kMaxBatch) return FA_ERR_UNSUPPORTED;
+  typedef cudaError_t (*Launcher)(const fa::VarlenMaps&, const fa::VarlenArgs&, int,
+                                  cudaStream_t);
+  Launcher launch = nullptr;
+  if (d_qk == 64 && d_v == 64) launch = fa::launch_varlen_64_64;
+  else if (d_qk == 72 && d_v == 72) launch = fa::launch_varlen_72_72;
+  else if (d_qk == 80 && d_v == 80) launch = fa::launch_varlen_80_80;
+  else if (d_qk == 96 && d_v == 96) launch = fa::launch_varlen_96_96;
+  else if (d_qk == 128 && d_v == 128) launch = fa::launch_varlen_128_128;
+  else if (d_qk == 192 && d_v == 128) launch = fa::launch_varlen_192_128;
+  if (!launch) return FA_ERR_UNSUPPORTED;
+  // Token indices are 32-bit in the kernel.
+  if ((int64_t)total_q * num_heads > INT32_MAX || (int64_t)total_k * num_heads_k > INT32_MAX)
+    return FA_ERR_UNSUPPORTED;
+
+  DeviceInfo* dev = nullptr;
+  fa_status st = device_info(&dev);
+  if (st != FA_OK) return st;
+  if (total_q == 0) return FA_OK;
+
+  // ---- TMA descriptors (host-only encoding, no device interaction)
+  fa::VarlenMaps maps;
+  std::memset(&maps, 0, sizeof maps);
+  const void* kb = total_k > 0 ? k : q;  // never dereferenced when total_k == 0
+  const void* vb = total_k > 0 ? v : q;
+  const int kh = total_k > 0 ? num_heads_k : num_heads;
+  const int vd = total_k > 0 ? d_v : d_qk;
+  const int tk = total_k > 0 ? total_k : total_q;
+  const int qt = tail_width(d_qk), vt = tail_width(d_v);
+  bool ok = encode_rows(&maps.q_full, q, d_qk, num_heads, total_q, 64, fa::kBM) &&
+            encode_rows(&maps.k_full, kb, d_qk, kh, tk, 64, fa::kBN) &&
+            encode_rows(&maps.v_full, vb, vd, kh, tk, 64, fa::kBN);
+  if (ok && qt)
+    ok = encode_rows(&maps.q_tail, q, d_qk, num_heads, total_q, qt, fa::kBM) &&
+         encode_rows(&maps.k_tail, kb, d_qk, kh, tk, qt, fa::kBN);
+  if (ok && vt) ok = encode_rows(&maps.v_tail, vb, vd, kh, tk, vt, fa::kBN);
+  if (!ok) return FA_ERR_LAUNCH;
+
+  fa::VarlenArgs args;
+  args.cu_q = cu_seqlens_q;
+  args.cu_k = cu_seqlens_k;
+  args.batch = batch;
+  args.num_heads = num_heads;
+  args.num_heads_k = num_heads_k;
+  args.total_q = total_q;
+  args.scale_log2 = softmax_scale * 1.4426950408889634f;
+  args.wl = window_left;
+  // Causal is the window's right edge on the bottom-right diagonal
+  // (window_right >= -1, so min(window_right, 0) is 0 whenever causal).
+  args.wr = causal ? 0 : window_right;
+  args.out = static_cast<uint16_t*>(out);
+  args.lse = lse;
+  args.status = dev->status;
+
+  // Persistent grid: no more CTAs than SMs or than work items could exist.
+  const int64_t item_bound =
+      (int64_t)num_heads * ((total_q + fa::kRowsPerItem - 1) / fa::kRowsPerItem + batch);
+  int grid = (int)(item_bound < dev->sm_count ? item_bound : dev->sm_count);
+  if (grid < 1) grid = 1;
+  cudaError_t e = launch(maps, args, grid, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+extern "C" fa_status fa_sparse_mla_decode(const void* q, const void* kv_cache,
+                                          const int* page_table, const int* topk_idx,
+                                          int num_tokens, int num_heads, int topk,
+                                          int num_pages, int max_pages_per_tok,
+                                          float softmax_scale, void* out, float* lse,
+                                          fa_stream_t stream) {
+  if (!q || !kv_cache || !page_table || !topk_idx || !out) return FA_ERR_INVALID_ARG;
+  if (num_tokens < 0 || num_pages < 1 || max_pages_per_tok < 1 || topk < 1)
+    return FA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(page_table, 4) ||
+      !aligned(topk_idx, 4) || (lse && !aligned(lse, 4)))
+    return FA_ERR_INVALID_ARG;
+  if (num_heads != 8 && num_heads != 16 && num_heads != 32 && num_heads != 64 &&
+      num_heads != 128)
+    return FA_ERR_UNSUPPORTED;
+  if (topk % 128 != 0 || (int64_t)topk > (int64_t)max_pages_per_tok * fa::kDecodePage)
+    return FA_ERR_UNSUPPORTED;
+  if ((int64_t)num_pages * fa::kDecodePage > INT32_MAX) return FA_ERR_UNSUPPORTED;
+  DeviceInfo* dev = nullptr;
+  fa_status st = device_info(&dev);
+  if (st != FA_OK) return st;
+  if (num_tokens == 0) return FA_OK;
+  fa::DecodeArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.cache = static_cast<const uint16_t*>(kv_cache);
+  a.page_table = page_table;
+  a.topk_idx = topk_idx;
+  a.num_tokens = num_tokens;
+  a.num_heads = num_heads;
+  a.topk = topk;
+  a.num_pages = num_pages;
+  a.max_pages = max_pages_per_tok;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.status = dev->status;
+  cudaError_t e = fa::launch_sparse_decode(a, dev->sm_count, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+extern "C" fa_status fa_get_device_status(void) {
+  DeviceInfo* dev = nullptr;
+  fa_status st = device_info(&dev);
+  if (st != FA_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_LAUNCH;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fa_status, sizeof v) != cudaSuccess) return FA_ERR_LAUNCH;
+  const unsigned int zero = 0;
+  if (cudaMemcpyToSymbol(g_fa_status, &zero, sizeof zero) != cudaSuccess) return FA_ERR_LAUNCH;
+  return (v & fa::kStatusTimeout) ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+}
+
+extern "C" const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_ARCH: return "device is not sm_103 (GB300)";
+    case FA_ERR_LAUNCH: return "CUDA launch or driver call failed";
+    case FA_ERR_DEVICE_TIMEOUT: return "a kernel pipeline wait timed out";
+  }
+  return "unknown status";
+}

@@ -1,0 +1,741 @@
+// varlen_fwd_kernel.cuh -- variable-length attention forward for sm_103a.
+//
+// One persistent CTA per SM walks a static, longest-first list of work items.
+// A work item is (sequence, head, pair of 128-row query tiles).  Per item:
+//
+//   producer warp   TMA: Q tiles once, then K_j, V_j tiles into a ring of
+//                   shared-memory slots guarded by mbarriers.
+//   MMA warp        tcgen05.mma (one elected thread):
+//                     S_t = Q_t K_jᵀ          (SS form, fp32 accumulator in TMEM)
+//                     O_t += P_t V_j          (TS form, P read from TMEM)
+//   softmax WG t    one thread per query row (TMEM lane): loads S_t, masks only
+//                   boundary tiles, 3-input max reduction, exp2, row sum,
+//                   lazy O rescale (threshold kRescaleLog2), writes P_t as bf16
+//                   into the S_t columns, and at the end normalises O_t and
+//                   stores O and the LSE.
+//
+// TMEM (512 columns x 128 lanes x 32 bit):
+//   [  0,128) S_0 / P_0   [128,256) S_1 / P_1   [256,384) O_0   [384,512) O_1
+//
+// Shared memory: Q_0, Q_1 tiles, NSTAGE ring slots (each holds one K or one V
+// tile), mbarriers, and the work list.  Every tile is stored as column chunks
+// of the head dimension, 64 bf16 wide with the 128-byte swizzle (or one
+// narrower tail chunk with the 32/64-byte swizzle), which is both the TMA
+// box layout and the UMMA canonical layout (K-major for Q and K, MN-major for
+// V).
+//
+// Method sources: sglang PR #41344 (FA4 path on Blackwell), "Motivation" and
+// "Modifications" (row max reduced in software over each 128-column S row;
+// exp2 after the max; rescale threshold; only tiles that need masking are
+// masked, and the first processed tile is a masked one); vLLM API page
+// "vllm.v1.attention.backends.mla.prefill.flash_attn", FA4MLAPrefillKernel
+// CompileKey (128-row query tile, q_stage of two tiles per CTA, static
+// persistent scheduler).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+constexpr int kVarlenThreads = 384;   // 2 softmax warpgroups + {producer, MMA, 2 idle} warps
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+// Register split (launch: 168 per thread x 384 threads = 64512):
+// softmax warpgroups 2 x 128 x 208 + control warpgroup 128 x 56 = 60416.
+constexpr uint32_t kSoftmaxRegs = 208;
+constexpr uint32_t kControlRegs = 56;
+constexpr int kBM = 128;              // query rows per tile
+constexpr int kBN = 128;              // keys per KV tile
+constexpr int kRowsPerItem = 2 * kBM; // two query tiles per work item
+constexpr int kMaxBatch = 1024;
+constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold, log2 units
+constexpr int kSmemBudget = 232448;   // 227 KB opt-in per CTA
+
+constexpr unsigned int kStatusTimeout = 1u;
+
+// Head-dim chunking: full 64-element chunks plus an optional 16- or 32-element
+// tail (dims padded to a multiple of 16 with TMA zero fill).
+template <int D>
+struct HeadDim {
+  static constexpr int padded = (D + 15) / 16 * 16;
+  static constexpr int full = padded / 64;
+  static constexpr int tail = padded % 64;  // 0, 16 or 32
+  static constexpr int chunks = full + (tail ? 1 : 0);
+  static_assert(tail == 0 || tail == 16 || tail == 32, "unsupported head dim");
+  // Byte offset of chunk c inside a tile of `rows` rows.
+  __host__ __device__ static constexpr int chunk_off(int c, int rows) { return c * rows * 128; }
+  __host__ __device__ static constexpr int chunk_width(int c) { return c < full ? 64 : tail; }
+  static constexpr int tile_bytes(int rows) { return rows * padded * 2; }
+};
+
+__host__ __device__ constexpr uint32_t layout_for_width(int w) {
+  return w == 64 ? ptx::kLayoutSw128 : (w == 32 ? ptx::kLayoutSw64 : ptx::kLayoutSw32);
+}
+
+template <int D_QK, int D_V>
+struct VarlenCfg {
+  using QK = HeadDim<D_QK>;
+  using VD = HeadDim<D_V>;
+  static constexpr int q_tile_bytes = QK::tile_bytes(kBM);
+  static constexpr int k_tile_bytes = QK::tile_bytes(kBN);
+  static constexpr int v_tile_bytes = VD::tile_bytes(kBN);
+  static constexpr int slot_bytes =
+      ((k_tile_bytes > v_tile_bytes ? k_tile_bytes : v_tile_bytes) + 1023) / 1024 * 1024;
+  static constexpr int sched_bytes_max = 8 * (kMaxBatch + 1) + 4 * kVarlenThreads;
+  static constexpr int fixed_bytes = 1024 /*align*/ + 2 * q_tile_bytes + 256 /*barriers*/;
+  static constexpr int nstage_fit = (kSmemBudget - fixed_bytes - sched_bytes_max) / slot_bytes;
+  static constexpr int nstage = nstage_fit > 8 ? 8 : nstage_fit;
+  static_assert(nstage >= 2, "shared memory too small for two ring slots");
+  static_assert(VD::padded <= 128, "O accumulator wider than its TMEM region");
+  // TMEM columns of the S/P and O regions of query tile t.
+  __host__ __device__ static constexpr uint32_t s_col(int t) { return 128u * (uint32_t)t; }
+  __host__ __device__ static constexpr uint32_t o_col(int t) { return 256u + 128u * (uint32_t)t; }
+};
+
+struct VarlenArgs {
+  const int* cu_q;
+  const int* cu_k;
+  int batch;
+  int num_heads;
+  int num_heads_k;
+  int total_q;
+  float scale_log2;  // softmax_scale * log2(e)
+  int wl;            // window left, -1 = unbounded
+  int wr;            // window right with causal folded in, -1 = unbounded
+  uint16_t* out;     // bf16 [total_q, H, d_v]
+  float* lse;        // [H, total_q] or null
+  unsigned int* status;
+};
+
+struct VarlenMaps {
+  CUtensorMap q_full, q_tail, k_full, k_tail, v_full, v_tail;
+};
+
+// Shared-memory control block (after the tiles).
+struct alignas(8) VarlenBarriers {
+  uint64_t q_full[2];
+  uint64_t q_free;
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full[2];
+  uint64_t o_free[2];
+  uint64_t drain;
+  uint64_t kv_full[8];
+  uint64_t kv_free[8];
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
+
+struct WorkItem {
+  int q_start, k_start, lq, lk, head, kv_head, row0, n_qt, tile_lo, n_kv;
+};
+
+// ------------------------------------------------------------ bounded waits
+// Wait time limit for any pipeline barrier.  Normal waits are microseconds;
+// hitting the limit means the pipeline is broken.  The kernel then records
+// kStatusTimeout, raises the CTA abort flag and unwinds instead of hanging.
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
+__device__ __forceinline__ bool wait_single(uint32_t bar, uint32_t parity,
+                                            volatile int* abort_flag, unsigned int* status) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t spin = 1;; ++spin) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((spin & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+        atomicOr(status, kStatusTimeout);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Warp-uniform variant: every lane of the warp gets the same answer, so the
+// warp stays converged for the warp-collective tcgen05 loads and stores.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
+                                          volatile int* abort_flag, unsigned int* status) {
+  const unsigned full = 0xffffffffu;
+  if (__all_sync(full, ptx::mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t spin = 1;; ++spin) {
+    if (__all_sync(full, ptx::mbar_try_wait(bar, parity))) return true;
+    if ((spin & 255u) == 0) {
+      int give_up = 0;
+      if ((threadIdx.x & 31) == 0) {
+        if (*abort_flag) {
+          give_up = 1;
+        } else if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+          atomicOr(status, kStatusTimeout);
+          *abort_flag = 1;
+          give_up = 1;
+        }
+      }
+      if (__shfl_sync(full, give_up, 0)) return false;
+    }
+  }
+}
+
+// ------------------------------------------------------------ work list
+// Builds, in shared memory, the sequences sorted by key length (longest
+// first, ties by index) and the prefix sum of their work-item counts.
+// The key array doubles as the prefix array once the ranks are known.
+__device__ __forceinline__ void build_work_list(const VarlenArgs& a, int* s_prefix,
+                                                int* s_sorted, int* s_part) {
+  const int tid = threadIdx.x;
+  const int B = a.batch;
+  int* s_key = s_prefix;
+  for (int b = tid; b < B; b += kVarlenThreads) s_key[b] = a.cu_k[b + 1] - a.cu_k[b];
+  __syncthreads();
+  for (int b = tid; b < B; b += kVarlenThreads) {
+    const int kb = s_key[b];
+    int rank = 0;
+    for (int o = 0; o < B; ++o) {
+      const int ko = s_key[o];
+      rank += (ko > kb) || (ko == kb && o < b);
+    }
+    s_sorted[rank] = b;
+  }
+  __syncthreads();
+  // Block-wide exclusive scan of per-sequence item counts in sorted order.
+  const int per = (B + kVarlenThreads - 1) / kVarlenThreads;
+  const int beg = tid * per;
+  const int end = min(B, beg + per);
+  int local = 0;
+  for (int p = beg; p < end; ++p) {
+    const int b = s_sorted[p];
+    const int lq = a.cu_q[b + 1] - a.cu_q[b];
+    local += a.num_heads * ((max(lq, 0) + kRowsPerItem - 1) / kRowsPerItem);
+  }
+  s_part[tid] = local;
+  __syncthreads();
+  if (tid < 32) {
+    // Warp 0 scans the kVarlenThreads partial sums, kPer per lane.
+    constexpr int kPer = (kVarlenThreads + 31) / 32;
+    int vals[kPer];
+    int run = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int idx = tid * kPer + i;
+      vals[i] = idx < kVarlenThreads ? s_part[idx] : 0;
+      run += vals[i];
+    }
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (tid >= o) incl += n;
+    }
+    int excl = incl - run;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int idx = tid * kPer + i;
+      if (idx < kVarlenThreads) s_part[idx] = excl;
+      excl += vals[i];
+    }
+  }
+  __syncthreads();
+  int run = s_part[tid];
+  for (int p = beg; p < end; ++p) {
+    s_prefix[p] = run;
+    const int b = s_sorted[p];
+    const int lq = a.cu_q[b + 1] - a.cu_q[b];
+    run += a.num_heads * ((max(lq, 0) + kRowsPerItem - 1) / kRowsPerItem);
+  }
+  if (end == B && beg < end) s_prefix[B] = run;  // the thread owning the last chunk
+  __syncthreads();
+}
+
+__device__ __forceinline__ WorkItem decode_item(int it, const VarlenArgs& a,
+                                                const int* s_prefix, const int* s_sorted) {
+  // Largest sorted position p with prefix[p] <= it (skips empty sequences).
+  int lo = 0, hi = a.batch - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_prefix[mid] <= it) lo = mid; else hi = mid - 1;
+  }
+  const int b = s_sorted[lo];
+  const int r = it - s_prefix[lo];
+  WorkItem w;
+  w.q_start = a.cu_q[b];
+  w.k_start = a.cu_k[b];
+  w.lq = a.cu_q[b + 1] - w.q_start;
+  w.lk = a.cu_k[b + 1] - w.k_start;
+  const int pairs = (w.lq + kRowsPerItem - 1) / kRowsPerItem;
+  w.head = r / pairs;
+  const int pair = pairs - 1 - (r - w.head * pairs);  // later rows first
+  w.kv_head = w.head / (a.num_heads / a.num_heads_k);
+  w.row0 = pair * kRowsPerItem;
+  const int row_end = min(w.lq, w.row0 + kRowsPerItem);
+  w.n_qt = (row_end - w.row0 + kBM - 1) / kBM;
+  const int off = w.lk - w.lq;
+  const int key_lo = a.wl >= 0 ? max(0, w.row0 + off - a.wl) : 0;
+  const int key_hi = a.wr >= 0 ? min(w.lk, row_end + off + a.wr) : w.lk;
+  if (key_hi <= key_lo) {
+    w.tile_lo = 0;
+    w.n_kv = 0;
+  } else {
+    w.tile_lo = key_lo / kBN;
+    w.n_kv = (key_hi + kBN - 1) / kBN - w.tile_lo;
+  }
+  return w;
+}
+
+// ------------------------------------------------------------ the kernel
+template <int D_QK, int D_V>
+__global__ void __launch_bounds__(kVarlenThreads, 1)
+    varlen_fwd_kernel(const __grid_constant__ VarlenMaps maps, const VarlenArgs args) {
+  using C = VarlenCfg<D_QK, D_V>;
+  using QK = typename C::QK;
+  using VD = typename C::VD;
+  constexpr int NS = C::nstage;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_tile[2] = {smem, smem + C::q_tile_bytes};
+  uint8_t* ring = smem + 2 * C::q_tile_bytes;
+  VarlenBarriers* cb = reinterpret_cast<VarlenBarriers*>(ring + NS * C::slot_bytes);
+  int* s_prefix = reinterpret_cast<int*>(cb + 1);
+  int* s_sorted = s_prefix + (args.batch + 1);
+  int* s_part = s_sorted + args.batch;
+  volatile int* abort_flag = &cb->abort_flag;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  if (tid == 0) {
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(ptx::smem_u32(&cb->q_full[t]), 1);
+      ptx::mbar_init(ptx::smem_u32(&cb->s_full[t]), 1);
+      ptx::mbar_init(ptx::smem_u32(&cb->p_full[t]), kBM);
+      ptx::mbar_init(ptx::smem_u32(&cb->o_full[t]), 1);
+      ptx::mbar_init(ptx::smem_u32(&cb->o_free[t]), kBM);
+    }
+    ptx::mbar_init(ptx::smem_u32(&cb->q_free), 1);
+    ptx::mbar_init(ptx::smem_u32(&cb->drain), 1);
+    for (int s = 0; s < NS; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&cb->kv_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&cb->kv_free[s]), 1);
+    }
+    cb->abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    ptx::prefetch_tmap(&maps.q_full);
+    ptx::prefetch_tmap(&maps.k_full);
+    ptx::prefetch_tmap(&maps.v_full);
+    if (QK::tail) {
+      ptx::prefetch_tmap(&maps.q_tail);
+      ptx::prefetch_tmap(&maps.k_tail);
+    }
+    if (VD::tail) ptx::prefetch_tmap(&maps.v_tail);
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(&cb->tmem_base), 512);
+    ptx::tmem_relinquish();
+  }
+  build_work_list(args, s_prefix, s_sorted, s_part);  // ends with __syncthreads
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = cb->tmem_base;
+  const int total_items = s_prefix[args.batch];
+
+  if (warp >= 8) {
+    ptx::regs_dec<kControlRegs>();
+    if (warp == kProducerWarp) {
+      // ---------------------------------------------------------- producer
+      if (lane == 0) {
+        uint32_t qf_n = 0;
+        int slot = 0;
+        uint32_t phase = 0;
+        uint32_t q_issued[2] = {0, 0};
+        uint32_t slot_issued[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        bool ok = true;
+        for (int it = blockIdx.x; it < total_items && ok; it += gridDim.x) {
+          const WorkItem w = decode_item(it, args, s_prefix, s_sorted);
+          if (w.n_kv == 0) continue;
+          ok = wait_single(ptx::smem_u32(&cb->q_free), (qf_n & 1) ^ 1, abort_flag, args.status);
+          ++qf_n;
+          if (!ok) break;
+          for (int t = 0; t < w.n_qt; ++t) {
+            const uint32_t bar = ptx::smem_u32(&cb->q_full[t]);
+            ptx::mbar_arrive_expect_tx(bar, C::q_tile_bytes);
+            ++q_issued[t];
+            const int row = w.q_start + w.row0 + t * kBM;
+#pragma unroll
+            for (int c = 0; c < QK::chunks; ++c)
+              ptx::tma_load_3d(ptx::smem_u32(q_tile[t] + QK::chunk_off(c, kBM)),
+                               c < QK::full ? &maps.q_full : &maps.q_tail, bar, c * 64, w.head,
+                               row);
+          }
+          for (int j = 0; j < w.n_kv && ok; ++j) {
+            const int krow = w.k_start + (w.tile_lo + j) * kBN;
+            for (int kind = 0; kind < 2; ++kind) {  // 0: K tile, 1: V tile
+              ok = wait_single(ptx::smem_u32(&cb->kv_free[slot]), phase ^ 1, abort_flag,
+                               args.status);
+              if (!ok) break;
+              const uint32_t bar = ptx::smem_u32(&cb->kv_full[slot]);
+              uint8_t* dst = ring + slot * C::slot_bytes;
+              if (kind == 0) {
+                ptx::mbar_arrive_expect_tx(bar, C::k_tile_bytes);
+#pragma unroll
+                for (int c = 0; c < QK::chunks; ++c)
+                  ptx::tma_load_3d(ptx::smem_u32(dst + QK::chunk_off(c, kBN)),
+                                   c < QK::full ? &maps.k_full : &maps.k_tail, bar, c * 64,
+                                   w.kv_head, krow);
+              } else {
+                ptx::mbar_arrive_expect_tx(bar, C::v_tile_bytes);
+#pragma unroll
+                for (int c = 0; c < VD::chunks; ++c)
+                  ptx::tma_load_3d(ptx::smem_u32(dst + VD::chunk_off(c, kBN)),
+                                   c < VD::full ? &maps.v_full : &maps.v_tail, bar, c * 64,
+                                   w.kv_head, krow);
+              }
+              ++slot_issued[slot];
+              if (++slot == NS) { slot = 0; phase ^= 1; }
+            }
+          }
+        }
+        if (!ok) {
+          // Let every copy this thread started land before the CTA exits.
+          for (int t = 0; t < 2; ++t)
+            if (q_issued[t])
+              wait_single(ptx::smem_u32(&cb->q_full[t]), (q_issued[t] - 1) & 1, abort_flag,
+                          args.status);
+          for (int s = 0; s < NS; ++s)
+            if (slot_issued[s])
+              wait_single(ptx::smem_u32(&cb->kv_full[s]), (slot_issued[s] - 1) & 1, abort_flag,
+                          args.status);
+        }
+      }
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(kBM, kBN, false, false);
+        constexpr uint32_t idesc_pv_full = ptx::idesc_bf16_f32(kBM, 64, false, true);
+        constexpr uint32_t idesc_pv_tail =
+            ptx::idesc_bf16_f32(kBM, VD::tail ? VD::tail : 16, false, true);
+        uint32_t qn[2] = {0, 0}, pn[2] = {0, 0}, ofn[2] = {0, 0};
+        int slot = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        bool issued_any = false;
+
+        auto issue_s = [&](int t, const uint8_t* kbuf) {
+          const uint32_t d = tmem + C::s_col(t);
+          const uint32_t qa = ptx::smem_u32(q_tile[t]);
+          const uint32_t ka = ptx::smem_u32(kbuf);
+#pragma unroll
+          for (int s = 0; s < QK::padded / 16; ++s) {
+            const int c = (s * 16) / 64;
+            const int w = QK::chunk_width(c);
+            const uint32_t in = ((s * 16) % 64) * 2;
+            const uint32_t sbo = 8 * w * 2;
+            const uint32_t lay = layout_for_width(w);
+            const uint64_t ad = ptx::smem_desc(qa + QK::chunk_off(c, kBM) + in, 16, sbo, lay);
+            const uint64_t bd = ptx::smem_desc(ka + QK::chunk_off(c, kBN) + in, 16, sbo, lay);
+            ptx::mma_ss(d, ad, bd, idesc_s, s > 0 ? 1u : 0u);
+          }
+        };
+        auto issue_pv = [&](int t, const uint8_t* vbuf, bool first) {
+          const uint32_t va = ptx::smem_u32(vbuf);
+#pragma unroll
+          for (int c = 0; c < VD::chunks; ++c) {
+            const int w = VD::chunk_width(c);
+            const uint32_t d = tmem + C::o_col(t) + c * 64;
+            const uint32_t sbo = 8 * w * 2;
+            const uint32_t lay = layout_for_width(w);
+            const uint32_t idesc = c < VD::full ? idesc_pv_full : idesc_pv_tail;
+#pragma unroll
+            for (int s = 0; s < kBN / 16; ++s) {
+              const uint32_t a_t = tmem + C::s_col(t) + s * 8;
+              // MN-major B with the MN extent (<= 64) inside one swizzle atom:
+              // only the 8-key-group stride matters; it is given in both
+              // offset fields.
+              const uint64_t bd =
+                  ptx::smem_desc(va + VD::chunk_off(c, kBN) + s * 16 * w * 2, sbo, sbo, lay);
+              ptx::mma_ts(d, a_t, bd, idesc, (!first || s > 0) ? 1u : 0u);
+            }
+          }
+        };
+
+        for (int it = blockIdx.x; it < total_items && ok; it += gridDim.x) {
+          const WorkItem w = decode_item(it, args, s_prefix, s_sorted);
+          if (w.n_kv == 0) continue;
+          issued_any = true;
+          const int nt = w.n_qt;
+          for (int t = 0; t < nt && ok; ++t) {
+            ok = wait_single(ptx::smem_u32(&cb->q_full[t]), qn[t] & 1, abort_flag, args.status);
+            ++qn[t];
+          }
+          if (!ok) break;
+          // Prologue: S_t(0) for both tiles.
+          ok = wait_single(ptx::smem_u32(&cb->kv_full[slot]), phase, abort_flag, args.status);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          {
+            const uint8_t* kbuf = ring + slot * C::slot_bytes;
+            for (int t = 0; t < nt; ++t) {
+              issue_s(t, kbuf);
+              ptx::mma_commit(ptx::smem_u32(&cb->s_full[t]));
+            }
+            ptx::mma_commit(ptx::smem_u32(&cb->kv_free[slot]));
+            if (w.n_kv == 1) ptx::mma_commit(ptx::smem_u32(&cb->q_free));
+            if (++slot == NS) { slot = 0; phase ^= 1; }
+          }
+          for (int j = 0; j < w.n_kv && ok; ++j) {
+            const int vslot = slot;
+            ok = wait_single(ptx::smem_u32(&cb->kv_full[vslot]), phase, abort_flag, args.status);
+            if (!ok) break;
+            if (++slot == NS) { slot = 0; phase ^= 1; }
+            const uint8_t* vbuf = ring + vslot * C::slot_bytes;
+            const bool has_next = j + 1 < w.n_kv;
+            int kslot = 0;
+            for (int t = 0; t < nt && ok; ++t) {
+              ok = wait_single(ptx::smem_u32(&cb->p_full[t]), pn[t] & 1, abort_flag, args.status);
+              ++pn[t];
+              if (!ok) break;
+              if (j == 0) {
+                ok = wait_single(ptx::smem_u32(&cb->o_free[t]), (ofn[t] & 1) ^ 1, abort_flag,
+                                 args.status);
+                ++ofn[t];
+                if (!ok) break;
+              }
+              ptx::tc_fence_after();
+              issue_pv(t, vbuf, j == 0);
+              if (has_next) {
+                if (t == 0) {
+                  kslot = slot;
+                  ok = wait_single(ptx::smem_u32(&cb->kv_full[kslot]), phase, abort_flag,
+                                   args.status);
+                  if (!ok) break;
+                  if (++slot == NS) { slot = 0; phase ^= 1; }
+                  ptx::tc_fence_after();
+                }
+                issue_s(t, ring + kslot * C::slot_bytes);
+                ptx::mma_commit(ptx::smem_u32(&cb->s_full[t]));
+              } else {
+                ptx::mma_commit(ptx::smem_u32(&cb->o_full[t]));
+              }
+            }
+            if (!ok) break;
+            if (has_next) {
+              ptx::mma_commit(ptx::smem_u32(&cb->kv_free[kslot]));
+              if (j + 2 == w.n_kv) ptx::mma_commit(ptx::smem_u32(&cb->q_free));
+            }
+            ptx::mma_commit(ptx::smem_u32(&cb->kv_free[vslot]));
+          }
+        }
+        if (issued_any) {
+          // Drain: every MMA issued by this thread completes before TMEM is freed.
+          ptx::mma_commit(ptx::smem_u32(&cb->drain));
+          wait_single(ptx::smem_u32(&cb->drain), 0, abort_flag, args.status);
+        }
+      }
+      __syncwarp();
+    }
+  } else {
+    ptx::regs_inc<kSoftmaxRegs>();
+    // ------------------------------------------------------------ softmax WG t
+    const int t = warp >> 2;                 // query tile of this warpgroup
+    const int row_in_tile = tid & 127;       // == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_addr = tmem + lane_base + C::s_col(t);
+    const uint32_t o_addr = tmem + lane_base + C::o_col(t);
+    const float sl2 = args.scale_log2;
+    const float neg_inf = -__int_as_float(0x7f800000);
+    uint32_t sn = 0, on = 0;
+    bool ok = true;
+
+    for (int it = blockIdx.x; it < total_items && ok; it += gridDim.x) {
+      const WorkItem w = decode_item(it, args, s_prefix, s_sorted);
+      if (t >= w.n_qt) continue;
+      const int i = w.row0 + t * kBM + row_in_tile;  // query row within the sequence
+      const bool row_valid = i < w.lq;
+      const int off = w.lk - w.lq;
+      int lo_i = 0, hi_i = 0;
+      if (row_valid) {
+        lo_i = args.wl >= 0 ? max(0, i + off - args.wl) : 0;
+        hi_i = args.wr >= 0 ? min(w.lk, i + off + args.wr + 1) : w.lk;
+        if (hi_i < lo_i) hi_i = lo_i;
+      }
+      float m_used = neg_inf;  // running max, scaled log2 units
+      float l = 0.f;
+      for (int j = 0; j < w.n_kv; ++j) {
+        ok = wait_warp(ptx::smem_u32(&cb->s_full[t]), sn & 1, abort_flag, args.status);
+        ++sn;
+        if (!ok) break;
+        ptx::tc_fence_after();
+        uint32_t sr[kBN];
+#pragma unroll
+        for (int q = 0; q < kBN / 32; ++q) ptx::tmem_ld32(s_addr + q * 32, sr + q * 32);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < kBN / 16; ++q) ptx::reg_fence16(sr + q * 16);
+        float s[kBN];
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) s[c] = __uint_as_float(sr[c]);
+
+        const int k0 = (w.tile_lo + j) * kBN;
+        if (!(k0 >= lo_i && k0 + kBN <= hi_i)) {
+          // Boundary tile for this row: mask keys outside [lo_i, hi_i).
+          const unsigned span = (unsigned)(hi_i - lo_i);
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            s[c] = ((unsigned)(k0 + c - lo_i) < span) ? s[c] : neg_inf;
+        }
+        // Row max: software reduction with 3-input max, 4 independent chains.
+        float mx[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mx[k] = fmaxf(s[k], s[k + 4]);
+#pragma unroll
+        for (int c = 8; c < kBN; c += 8) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mx[k] = ptx::max3(mx[k], s[c + k], s[c + k + 4]);
+        }
+        const float row_max = ptx::max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+        const float m_tile = row_max * sl2;  // -inf stays -inf
+        const bool need = m_tile > m_used + kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = fmaxf(m_used, m_tile);
+          const float alpha = (m_used == neg_inf) ? 0.f : ptx::ex2(m_used - m_new);
+          if (j > 0) {
+            // O_t holds the sum of the earlier tiles (its PV has completed:
+            // the commit that released this S tile came after it).
+#pragma unroll
+            for (int c0 = 0; c0 < VD::padded; c0 += 16) {
+              uint32_t o[16];
+              ptx::tmem_ld16(o_addr + c0, o);
+              ptx::tmem_wait_ld();
+              ptx::reg_fence16(o);
+#pragma unroll
+              for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+              ptx::tmem_st16(o_addr + c0, o);
+            }
+          }
+          if (m_new != neg_inf) {
+            l *= alpha;
+            m_used = m_new;
+          }
+        }
+        const float base = (m_used == neg_inf) ? 0.f : m_used;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pr[kBN / 2];
+#pragma unroll
+        for (int c = 0; c < kBN; c += 2) {
+          const float p0 = ptx::ex2(fmaf(s[c], sl2, -base));
+          const float p1 = ptx::ex2(fmaf(s[c + 1], sl2, -base));
+          ls[(c >> 1) & 3] += p0 + p1;
+          pr[c >> 1] = ptx::pack_bf16x2(p0, p1);
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+#pragma unroll
+        for (int q = 0; q < kBN / 2; q += 32) ptx::tmem_st32(s_addr + q, pr + q);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(ptx::smem_u32(&cb->p_full[t]));
+      }
+      if (!ok) break;
+
+      // ---- epilogue: O / l -> bf16 rows, LSE
+      uint32_t o[VD::padded];
+      if (w.n_kv > 0) {
+        ok = wait_warp(ptx::smem_u32(&cb->o_full[t]), on & 1, abort_flag, args.status);
+        ++on;
+        if (!ok) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < VD::padded; c0 += 16) ptx::tmem_ld16(o_addr + c0, o + c0);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int c0 = 0; c0 < VD::padded; c0 += 16) ptx::reg_fence16(o + c0);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(ptx::smem_u32(&cb->o_free[t]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < VD::padded; ++c) o[c] = 0u;
+      }
+      if (row_valid) {
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const size_t tok = (size_t)(w.q_start + i);
+        uint4* dst = reinterpret_cast<uint4*>(args.out +
+                                              (tok * args.num_heads + w.head) * (size_t)D_V);
+#pragma unroll
+        for (int g = 0; g < D_V / 8; ++g) {
+          uint4 v;
+          v.x = ptx::pack_bf16x2(__uint_as_float(o[8 * g + 0]) * inv_l,
+                                 __uint_as_float(o[8 * g + 1]) * inv_l);
+          v.y = ptx::pack_bf16x2(__uint_as_float(o[8 * g + 2]) * inv_l,
+                                 __uint_as_float(o[8 * g + 3]) * inv_l);
+          v.z = ptx::pack_bf16x2(__uint_as_float(o[8 * g + 4]) * inv_l,
+                                 __uint_as_float(o[8 * g + 5]) * inv_l);
+          v.w = ptx::pack_bf16x2(__uint_as_float(o[8 * g + 6]) * inv_l,
+                                 __uint_as_float(o[8 * g + 7]) * inv_l);
+          dst[g] = v;
+        }
+        if (args.lse) {
+          // Natural-log LSE: (m + log2 l) * ln 2.
+          const float lse = l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : neg_inf;
+          args.lse[(size_t)w.head * args.total_q + tok] = lse;
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// Dynamic shared memory a launch needs for a given batch.
+template <int D_QK, int D_V>
+inline size_t varlen_smem_bytes(int batch) {
+  using C = VarlenCfg<D_QK, D_V>;
+  return (size_t)1024 + 2 * C::q_tile_bytes + (size_t)C::nstage * C::slot_bytes +
+         sizeof(VarlenBarriers) + 8 * (size_t)(batch + 1) + 4 * kVarlenThreads + 16;
+}
+
+// Launches one instantiation.  The dynamic shared-memory limit is raised once
+// per device to the size needed for the largest supported batch.
+template <int D_QK, int D_V>
+cudaError_t launch_varlen_impl(const VarlenMaps& maps, const VarlenArgs& args, int grid,
+                               cudaStream_t stream) {
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev]) {
+    e = cudaFuncSetAttribute(varlen_fwd_kernel<D_QK, D_V>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)varlen_smem_bytes<D_QK, D_V>(kMaxBatch));
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  const size_t smem = varlen_smem_bytes<D_QK, D_V>(args.batch);
+  varlen_fwd_kernel<D_QK, D_V><<<grid, kVarlenThreads, smem, stream>>>(maps, args);
+  return cudaGetLastError();
+}
+
+}  // namespace fa
+
+#define FA_DEFINE_VARLEN_LAUNCHER(DQK, DV)                                              \
+  namespace fa {                                                                         \
+  cudaError_t launch_varlen_##DQK##_##DV(const VarlenMaps& maps, const VarlenArgs& args, \
+                                         int grid, cudaStream_t stream) {               \
+    return launch_varlen_impl<DQK, DV>(maps, args, grid, stream);                        \
+  }                                                                                      \
+  }
