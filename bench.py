@@ -1,0 +1,369 @@
+"""Benchmark: varlen attention forward TFLOPS and fraction of the GB300 roofline.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                        [--workload NAME] [--extra] [--no-cpu-baseline]
+
+One step = one fa_varlen_fwd call over the whole packed batch of the
+workload (default: ViT encoder attention, packed images [576, 1024, 2304,
+4096, 256, 9216], 16 heads, head dim 80, non-causal).  Inputs are resident in
+HBM before timing; L2 is flushed (a 512 MB write) before every timed step and
+outside its CUDA-event pair.  Prints one JSON line on rank 0.
+
+`--impl reference` times the fp64 CPU oracle (the only reference arm this
+method has) on a bounded sample of the same workload and prints the same
+line with "impl": "reference".
+
+Multi-GPU: the path has no exchange step, so N > 1 runs N independent
+replicas (one per rank, launched by torchrun); the timed region is bracketed
+by barriers and the maximum over ranks is taken.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+REPO = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, REPO)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from varlen_flashattention_forward_gb300 import metrics, workloads  # noqa: E402
+
+METRIC = "varlen attention fwd TFLOPS and % of GB300 BF16 tensor peak (decode: % HBM BW)"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    path = os.path.join(REPO, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p.get("hbm_gbs", 6800.0), "bf16_tflops": p.get("bf16_tflops", 1900.0),
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", 1700.0),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, sm_max, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                sm_max = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": sm_max,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle timing
+def oracle_sample_rate(w, budget_s: float, seed: int = 0):
+    """Times the fp64 oracle on a random sample of (token, head) rows of the
+    workload; returns (flops/s, rows, seconds, threads)."""
+    import oracle
+    q, k, v, cq, ck = w.make_inputs()
+    rng = np.random.default_rng(seed)
+    counts = np.concatenate([metrics.visible_keys_per_row(lq, lk, w.causal, *w.window)
+                             for lq, lk in zip(w.lens_q, w.lens_k)])
+    n_rows_total = w.total_q * w.num_heads
+
+    def run(n):
+        rows = np.sort(rng.choice(n_rows_total, size=n, replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.varlen_attention(q, k, v, cq, ck, w.softmax_scale, w.causal, *w.window, rows=rows)
+        dt = time.perf_counter() - t0
+        flops = 2.0 * float(counts[rows // w.num_heads].sum()) * (w.d_qk + w.d_v)
+        return flops, dt, n
+
+    flops, dt, n = run(256)
+    target = max(256, min(n_rows_total, int(n * budget_s / max(dt, 1e-3))))
+    flops, dt, n = run(target)
+    return flops / dt, n, dt, oracle.num_threads()
+
+
+# ------------------------------------------------------------ GPU timing
+def time_varlen(w, steps, warmup, device, world):
+    import varlen_flashattention_forward_gb300 as fa
+    q, k, v, cq, ck = w.make_inputs()
+    qd, kd, vd, cqd, ckd = (t.to(device) for t in (q, k, v, cq, ck))
+    out = torch.empty((w.total_q, w.num_heads, w.d_v), dtype=torch.bfloat16, device=device)
+    lse = (torch.empty((w.num_heads, w.total_q), dtype=torch.float32, device=device)
+           if w.return_lse else None)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    args = (qd, kd, vd, cqd, ckd, max(w.lens_q), max(w.lens_k), w.softmax_scale, w.causal,
+            w.window[0], w.window[1], out, lse)
+    for _ in range(warmup):
+        fa.fa_varlen_fwd(*args)
+    torch.cuda.synchronize(device)
+    if fa.fa_get_device_status() != fa.FA_OK:
+        raise RuntimeError("device status word set during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize(device)
+    with ClockSampler(device.index or 0) as clk:
+        for i in range(steps):
+            flush.fill_(float(i))                     # evict inputs from L2
+            starts[i].record(stream)
+            fa.fa_varlen_fwd(*args)
+            ends[i].record(stream)
+        torch.cuda.synchronize(device)
+    barrier(world)
+    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+    # End to end through the public API with host buffers: pinned host inputs
+    # copied in, kernel, output copied back, every step.
+    hq, hk, hv, hcq, hck = (t.pin_memory() for t in (q, k, v, cq, ck))
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hcq, hck))
+    d2h = hout.numel() * hout.element_size()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(steps, 10))
+    for _ in range(2):
+        fa.fa_varlen_fwd(*args)
+    torch.cuda.synchronize(device)
+    e_start.record(stream)
+    for _ in range(e2e_steps):
+        qd.copy_(hq, non_blocking=True)
+        kd.copy_(hk, non_blocking=True)
+        vd.copy_(hv, non_blocking=True)
+        cqd.copy_(hcq, non_blocking=True)
+        ckd.copy_(hck, non_blocking=True)
+        fa.fa_varlen_fwd(*args)
+        hout.copy_(out, non_blocking=True)
+    e_end.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = e_start.elapsed_time(e_end) / e2e_steps
+    if fa.fa_get_device_status() != fa.FA_OK:
+        raise RuntimeError("device status word set during timing")
+    return times_ms, clk.summary(), e2e_ms, h2d, d2h
+
+
+def time_decode(d, steps, warmup, device):
+    """Device time of fa_sparse_mla_decode on the decode workload (inputs drawn
+    on the device for speed; parity is covered by the tests)."""
+    import varlen_flashattention_forward_gb300 as fa
+    page_table, topk = d.make_indices()
+    g = torch.Generator(device=device).manual_seed(d.seed)
+    cache = torch.randn((d.num_pages, 64, 576), generator=g, device=device).bfloat16()
+    q = torch.randn((d.num_tokens, d.num_heads, 576), generator=g, device=device).bfloat16()
+    pt, ti = page_table.to(device), topk.to(device)
+    out = torch.empty((d.num_tokens, d.num_heads, 512), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((d.num_heads, d.num_tokens), dtype=torch.float32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    for _ in range(warmup):
+        fa.fa_sparse_mla_decode(q, cache, pt, ti, d.softmax_scale, out, lse)
+    torch.cuda.synchronize(device)
+    ts = []
+    for i in range(steps):
+        flush.fill_(float(i))
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        fa.fa_sparse_mla_decode(q, cache, pt, ti, d.softmax_scale, out, lse)
+        e.record()
+        torch.cuda.synchronize(device)
+        ts.append(s.elapsed_time(e))
+    del cache
+    return ts
+
+
+def extra_lines(steps, warmup, device, peaks):
+    """Secondary workloads (not the headline): device time, TFLOPS, roofline."""
+    res = {}
+    for name in ["vit_window_d80", "vit_full_d128", "long_16384", "mla_causal", "mla_chunked",
+                 "mla_swa"]:
+        w = workloads.VARLEN_BENCH[name]()
+        try:
+            t, _, _, _, _ = time_varlen(w, steps, warmup, device, 1)
+        except Exception as exc:  # report and continue with the rest
+            res[name] = {"error": str(exc)[:200]}
+            continue
+        ms = statistics.mean(t)
+        flops = metrics.varlen_flops(w)
+        byts = metrics.varlen_alg_bytes(w)
+        t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
+        res[name] = {"ms": round(ms, 4), "tflops": round(flops / ms / 1e9, 1),
+                     "gbs": round(byts / ms / 1e6, 1),
+                     "roofline_frac": round(t_roof * 1e3 / ms, 4)}
+    try:
+        d = workloads.DecodeWorkload()
+        t = time_decode(d, steps, warmup, device)
+        ms = statistics.mean(t)
+        byts = metrics.decode_alg_bytes(d)
+        res["decode"] = {"ms": round(ms, 4), "gbs": round(byts / ms / 1e6, 1),
+                         "hbm_frac": round(byts / ms / 1e6 / peaks["hbm_gbs"], 4),
+                         "tflops": round(metrics.decode_flops(d) / ms / 1e9, 1)}
+    except Exception as exc:
+        res["decode"] = {"error": str(exc)[:200]}
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="vit_full_d80")
+    ap.add_argument("--extra", action="store_true", help="also time the other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    a = ap.parse_args()
+    a.warmup = max(a.warmup, 3)
+
+    world, rank, local = dist_setup()
+    w = workloads.VARLEN_BENCH[a.workload]()
+    peaks = load_peaks()
+    flops = metrics.varlen_flops(w)
+    byts = metrics.varlen_alg_bytes(w)
+    config = {"workload": w.name, "lens": w.lens_q, "num_heads": w.num_heads,
+              "d_qk": w.d_qk, "d_v": w.d_v, "causal": w.causal, "window": list(w.window),
+              "return_lse": w.return_lse, "l2": "flushed before every timed step (512 MB write)",
+              "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+    if a.impl == "reference":
+        if rank != 0:
+            return
+        rates = []
+        for s in range(a.warmup + a.steps):
+            rate, n, dt, threads = oracle_sample_rate(w, budget_s=a.cpu_budget / 4, seed=s)
+            if s >= a.warmup:
+                rates.append(rate)
+        val = statistics.mean(rates) / 1e12
+        ms = flops / (val * 1e12) * 1e3
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config,
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{n} random (token, head) rows per step, fp64 oracle, "
+                                       f"scaled to the workload's flop count"},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}))
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the product has no CPU path)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import varlen_flashattention_forward_gb300 as fa
+    fa.load_library()
+
+    times_ms, clocks, e2e_ms, h2d, d2h = time_varlen(w, a.steps, a.warmup, device, world)
+    ms = statistics.mean(times_ms)
+    ms = max_over_ranks(ms, world)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    if rank != 0:
+        return
+    tflops = flops / (ms * 1e-3) / 1e12 * world
+    achieved = flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
+                     "peak_source": peaks["source"] + " bf16 burst",
+                     "kernel": "varlen_fwd_kernel<%d,%d>" % (w.d_qk, w.d_v),
+                     "alg_flops_per_launch": flops, "alg_bytes_per_launch": byts},
+        "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": a.steps,
+        "clocks": clocks,
+        "ms_per_step_min": round(min(times_ms), 5),
+        "ms_per_step_median": round(statistics.median(times_ms), 5),
+    }
+    if not a.no_cpu_baseline:
+        rate, n, dt, threads = oracle_sample_rate(w, budget_s=a.cpu_budget)
+        line["cpu_baseline"] = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"{n} random (token, head) rows, {dt:.1f} s, fp64"}
+    if a.extra:
+        line["extra"] = extra_lines(max(3, a.steps // 4), 3, device, peaks)
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()
