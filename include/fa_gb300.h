@@ -121,7 +121,8 @@ fa_status fa_varlen_fwd(const void* q, const void* k, const void* v,
  *                 A slot with p < 0, p >= 64*max_pages_per_tok or a page id
  *                 outside [0, num_pages) is skipped (contributes nothing).
  *   num_heads     one of 8, 16, 32, 64, 128
- *   topk          multiple of 128, 128 .. 64*max_pages_per_tok
+ *   topk          multiple of 128, 128 .. min(2048, 64*max_pages_per_tok)
+ *                 (the per-token row table is held in shared memory)
  *   softmax_scale scale of the 576-wide dot product (> 0)
  *   out           bf16 [num_tokens, num_heads, 512]: sum_j p_j * row_j[0:512]
  *   lse           fp32 [num_heads, num_tokens] or NULL

@@ -1,0 +1,99 @@
+"""GPU parity of fa_sparse_mla_decode (through the C ABI) against the fp64
+oracle: max |O| error <= 2e-2 (bf16 output), max |LSE| error <= 1e-3."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import varlen_flashattention_forward_gb300 as fa
+from varlen_flashattention_forward_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 2e-2
+LSE_TOL = 1e-3
+
+
+def run_gpu(q, cache, pt, ti, scale):
+    dev = torch.device("cuda:0")
+    out, lse = fa.fa_sparse_mla_decode(q.to(dev), cache.to(dev), pt.to(dev), ti.to(dev), scale,
+                                       return_lse=True)
+    torch.cuda.synchronize()
+    return out.cpu(), lse.cpu()
+
+
+def compare(q, cache, pt, ti, scale, rows=None, out=None, lse=None):
+    if out is None:
+        out, lse = run_gpu(q, cache, pt, ti, scale)
+    ref_o, ref_l = oracle.sparse_mla_decode(q, cache, pt, ti, scale, rows=rows)
+    T, H, _ = out.shape
+    go = out.float().numpy().reshape(T * H, 512)
+    gl = lse.numpy().T.reshape(T * H)
+    if rows is not None:
+        go, gl = go[rows], gl[rows]
+    fin = np.isfinite(ref_l)
+    assert np.array_equal(np.isfinite(gl), fin)
+    err_o = float(np.abs(go - ref_o).max())
+    err_l = float(np.abs(gl[fin] - ref_l[fin]).max()) if fin.any() else 0.0
+    assert err_o <= O_TOL, f"max|dO| = {err_o}"
+    assert err_l <= LSE_TOL, f"max|dLSE| = {err_l}"
+    return err_o, err_l
+
+
+def small_inputs(T, H, topk, context, seed, num_pages=None):
+    d = workloads.small_decode(num_tokens=T, num_heads=H, topk=topk, context=context,
+                               num_pages=num_pages, seed=seed)
+    pt, ti = d.make_indices()
+    return d.make_q(), d.make_cache(), pt, ti, d.softmax_scale
+
+
+@pytest.mark.parametrize("H", [8, 16, 32, 64, 128])
+def test_head_counts_elementwise(cuda_device, H):
+    q, cache, pt, ti, scale = small_inputs(3, H, 256, 1024, seed=H)
+    compare(q, cache, pt, ti, scale)
+
+
+@pytest.mark.parametrize("topk", [128, 384, 2048])
+def test_topk_sizes_elementwise(cuda_device, topk):
+    q, cache, pt, ti, scale = small_inputs(2, 64, topk, 4096, seed=topk)
+    compare(q, cache, pt, ti, scale)
+
+
+def test_invalid_slots_are_skipped(cuda_device):
+    q, cache, pt, ti, scale = small_inputs(4, 64, 256, 1024, seed=7)
+    ti = ti.clone()
+    ti[0, ::7] = -1                    # negative position
+    ti[1, 5:40] = 1024 + 3             # past the context
+    pt = pt.clone()
+    pt[2, :] = -5                      # every page of token 2 out of range
+    compare(q, cache, pt, ti, scale)
+    out, lse = run_gpu(q, cache, pt, ti, scale)
+    assert torch.all(out[2] == 0) and torch.all(torch.isneginf(lse[:, 2]))
+
+
+def test_large_score_range_rescales(cuda_device):
+    q, cache, pt, ti, scale = small_inputs(2, 64, 512, 2048, seed=9)
+    q = (q.float() * 4).bfloat16()
+    compare(q, cache, pt, ti, scale)
+
+
+def test_bitwise_deterministic(cuda_device):
+    q, cache, pt, ti, scale = small_inputs(4, 64, 512, 2048, seed=11)
+    a = run_gpu(q, cache, pt, ti, scale)
+    b = run_gpu(q, cache, pt, ti, scale)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_full_size_sampled_rows(cuda_device):
+    """128 tokens, 64 heads, top-k 2048 of 32768 positions, 65536 pages."""
+    d = workloads.DecodeWorkload()
+    pt, ti = d.make_indices()
+    q = d.make_q()
+    cache = d.make_cache()
+    out, lse = run_gpu(q, cache, pt, ti, d.softmax_scale)
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([
+        rng.integers(0, d.num_tokens * d.num_heads, size=384),
+        np.arange(d.num_heads), (d.num_tokens - 1) * d.num_heads + np.arange(d.num_heads)]))
+    compare(q, cache, pt, ti, d.softmax_scale, rows=rows, out=out, lse=lse)
+    assert fa.fa_get_device_status() == fa.FA_OK
