@@ -280,6 +280,14 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
   return d;
 }
 
+// Descriptor advanced by `bytes` (a multiple of 16): only the start-address
+// field changes.  Shared addresses stay below 256 KB, so the 14-bit field
+// cannot carry into the leading-offset field.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
+  const uint32_t lo = (uint32_t)d + (bytes >> 4);
+  return ((d >> 32) << 32) | lo;
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
 //   bits 4..5 D format (1 = f32), 7..9 A format (1 = bf16), 10..12 B format
 //   (1 = bf16), bit 15 A major (0 = K-major, 1 = MN-major), bit 16 B major,

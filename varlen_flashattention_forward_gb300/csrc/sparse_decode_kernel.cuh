@@ -212,14 +212,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     ptx::regs_dec<kDecodeGatherRegs>();
     // ------------------------------------------------------------ gather
     const int ptid = tid - 128;
+    // Tile j goes to stage j % 2.  Each gather thread's copies of tile j
+    // arrive on r_full[j % 2] by themselves when they land
+    // (cp.async.mbarrier.arrive.noinc; the barrier expects 128 arrivals), so
+    // no gather warp ever blocks on its own copies.  Stage reuse for tile j
+    // waits for PV(j - 2), which needs only tiles <= j - 1.
     bool ok = true;
     for (int j = 0; j < n_tiles && ok; ++j) {
-      const int s = j & 1;
       if (j >= 2) {
-        ok = wait_warp(ptx::smem_u32(&cb->r_free[s]), ((j >> 1) - 1) & 1, abort_flag, a.status);
+        ok = wait_warp(ptx::smem_u32(&cb->r_free[j & 1]), ((j >> 1) - 1) & 1, abort_flag,
+                       a.status);
         if (!ok) break;
       }
-      const uint32_t dst0 = ptx::smem_u32(stage[s]);
+      const uint32_t dst0 = ptx::smem_u32(stage[j & 1]);
       const int* trow = rows + j * kDecodeKeys;
 #pragma unroll 4
       for (int e = ptid; e < kDecodeKeys * 72; e += 128) {
@@ -231,18 +236,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const uint32_t dst = dst0 + chunk * kChunkBytes + r * 128 + ((u ^ (r & 7)) << 4);
         ptx::cp_async_16(dst, src);
       }
-      cp_async_commit();
-      if (j >= 1) {
-        cp_async_wait<1>();
-        ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(ptx::smem_u32(&cb->r_full[(j - 1) & 1]));
-      }
+      ptx::cp_async_mbar_arrive(ptx::smem_u32(&cb->r_full[j & 1]));
     }
-    cp_async_wait<0>();
-    if (ok) {
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(ptx::smem_u32(&cb->r_full[(n_tiles - 1) & 1]));
-    }
+    cp_async_wait<0>();  // nothing of this thread is in flight at exit
   } else if (warp >= 8) {
     ptx::regs_dec<kDecodeControlRegs>();
     // ------------------------------------------------------------ MMA issuer
@@ -270,6 +266,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       };
       if (ok) ok = wait_single(ptx::smem_u32(&cb->r_full[0]), 0, abort_flag, a.status);
       if (ok) {
+        // The gathered rows were written by cp.async (generic proxy); order
+        // them before the tensor core's (async proxy) reads.
+        ptx::fence_proxy_async_smem();
         ptx::tc_fence_after();
         issue_s(0);
         ptx::mma_commit(ptx::smem_u32(&cb->s_full[0]));
@@ -279,6 +278,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           ok = wait_single(ptx::smem_u32(&cb->r_full[(j + 1) & 1]), ((j + 1) >> 1) & 1, abort_flag,
                            a.status);
           if (!ok) break;
+          ptx::fence_proxy_async_smem();
           ptx::tc_fence_after();
           issue_s(j + 1);
           ptx::mma_commit(ptx::smem_u32(&cb->s_full[(j + 1) & 1]));

@@ -431,40 +431,73 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         bool ok = true;
         bool issued_any = false;
 
+        // Descriptors are built once per buffer; each MMA then only adds a
+        // constant byte offset to the start-address field (this thread
+        // shares its issue slots with two softmax warps, so the per-MMA
+        // instruction count matters).
+        constexpr uint32_t kQkTailSbo = 8 * (QK::tail ? QK::tail : 16) * 2;
+        constexpr uint32_t kQkTailLay = layout_for_width(QK::tail ? QK::tail : 16);
+        constexpr uint32_t kVTailSbo = 8 * (VD::tail ? VD::tail : 16) * 2;
+        constexpr uint32_t kVTailLay = layout_for_width(VD::tail ? VD::tail : 16);
+        uint64_t q_desc[2], q_desc_tail[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const uint32_t qa = ptx::smem_u32(q_tile[t]);
+          q_desc[t] = ptx::smem_desc(qa, 16, 1024, ptx::kLayoutSw128);
+          q_desc_tail[t] =
+              ptx::smem_desc(qa + QK::chunk_off(QK::full, kBM), 16, kQkTailSbo, kQkTailLay);
+        }
         auto issue_s = [&](int t, const uint8_t* kbuf) {
           const uint32_t d = tmem + C::s_col(t);
-          const uint32_t qa = ptx::smem_u32(q_tile[t]);
           const uint32_t ka = ptx::smem_u32(kbuf);
+          const uint64_t kd = ptx::smem_desc(ka, 16, 1024, ptx::kLayoutSw128);
+          const uint64_t kd_tail =
+              ptx::smem_desc(ka + QK::chunk_off(QK::full, kBN), 16, kQkTailSbo, kQkTailLay);
 #pragma unroll
           for (int s = 0; s < QK::padded / 16; ++s) {
             const int c = (s * 16) / 64;
-            const int w = QK::chunk_width(c);
-            const uint32_t in = ((s * 16) % 64) * 2;
-            const uint32_t sbo = 8 * w * 2;
-            const uint32_t lay = layout_for_width(w);
-            const uint64_t ad = ptx::smem_desc(qa + QK::chunk_off(c, kBM) + in, 16, sbo, lay);
-            const uint64_t bd = ptx::smem_desc(ka + QK::chunk_off(c, kBN) + in, 16, sbo, lay);
-            ptx::mma_ss(d, ad, bd, idesc_s, s > 0 ? 1u : 0u);
+            if (c < QK::full) {
+              // kBM == kBN: the same offset addresses Q and K chunks.
+              const uint32_t off = (uint32_t)(QK::chunk_off(c, kBN) + ((s * 16) % 64) * 2);
+              ptx::mma_ss(d, ptx::desc_add(q_desc[t], off), ptx::desc_add(kd, off), idesc_s,
+                          s > 0 ? 1u : 0u);
+            } else {
+              const uint32_t off = (uint32_t)((s * 16 - QK::full * 64) * 2);
+              ptx::mma_ss(d, ptx::desc_add(q_desc_tail[t], off), ptx::desc_add(kd_tail, off),
+                          idesc_s, s > 0 ? 1u : 0u);
+            }
           }
         };
         auto issue_pv = [&](int t, const uint8_t* vbuf, bool first) {
           const uint32_t va = ptx::smem_u32(vbuf);
+          const uint32_t a0 = tmem + C::s_col(t);
+          if (VD::tail == 0) {
+            // One MMA per 16 keys over all of d_v: MN-major B spanning
+            // VD::full 64-wide atoms, VD::chunk_off(1, kBN) bytes apart.
+            constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(kBM, VD::padded, false, true);
+            const uint64_t vd =
+                ptx::smem_desc(va, VD::chunk_off(1, kBN), 1024, ptx::kLayoutSw128);
 #pragma unroll
-          for (int c = 0; c < VD::chunks; ++c) {
-            const int w = VD::chunk_width(c);
-            const uint32_t d = tmem + C::o_col(t) + c * 64;
-            const uint32_t sbo = 8 * w * 2;
-            const uint32_t lay = layout_for_width(w);
-            const uint32_t idesc = c < VD::full ? idesc_pv_full : idesc_pv_tail;
+            for (int s = 0; s < kBN / 16; ++s)
+              ptx::mma_ts(tmem + C::o_col(t), a0 + s * 8, ptx::desc_add(vd, s * 16 * 128),
+                          idesc_pv, (!first || s > 0) ? 1u : 0u);
+          } else {
+            // A 64-wide chunk (or none) plus a narrower tail chunk with its own
+            // swizzle.  For the MN extent inside one atom only the 8-key-group
+            // stride matters; it is given in both offset fields.
+            const uint64_t vd = ptx::smem_desc(va, 1024, 1024, ptx::kLayoutSw128);
+            const uint64_t vd_tail =
+                ptx::smem_desc(va + VD::chunk_off(VD::full, kBN), kVTailSbo, kVTailSbo, kVTailLay);
 #pragma unroll
             for (int s = 0; s < kBN / 16; ++s) {
-              const uint32_t a_t = tmem + C::s_col(t) + s * 8;
-              // MN-major B with the MN extent (<= 64) inside one swizzle atom:
-              // only the 8-key-group stride matters; it is given in both
-              // offset fields.
-              const uint64_t bd =
-                  ptx::smem_desc(va + VD::chunk_off(c, kBN) + s * 16 * w * 2, sbo, sbo, lay);
-              ptx::mma_ts(d, a_t, bd, idesc, (!first || s > 0) ? 1u : 0u);
+#pragma unroll
+              for (int c = 0; c < VD::full; ++c)
+                ptx::mma_ts(tmem + C::o_col(t) + c * 64, a0 + s * 8,
+                            ptx::desc_add(vd, VD::chunk_off(c, kBN) + s * 16 * 128),
+                            idesc_pv_full, (!first || s > 0) ? 1u : 0u);
+              ptx::mma_ts(tmem + C::o_col(t) + VD::full * 64, a0 + s * 8,
+                          ptx::desc_add(vd_tail, s * 16 * VD::tail * 2), idesc_pv_tail,
+                          (!first || s > 0) ? 1u : 0u);
             }
           }
         };
