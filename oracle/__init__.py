@@ -9,6 +9,7 @@ compiles it with gcc and marshals arrays through ctypes.
 Functions:
   varlen_attention(...)   -> (out [rows, d_v] f64, lse [rows] f64)
   sparse_mla_decode(...)  -> (out [rows, 512] f64, lse [rows] f64)
+  merge_states(...)       -> (out [rows, d] f64, lse [rows] f64)
 Rows are (token, head) pairs flattened as token * H + head.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
@@ -59,6 +60,8 @@ def _load():
                 p, p, p, p, i32, i32, i32, i32, i32, i32, f64, i64, p, p, p,
                 i32]
             lib.oracle_sparse_mla_decode.restype = i32
+            lib.oracle_merge_states.argtypes = [p, p, p, p, i64, i32, p, p]
+            lib.oracle_merge_states.restype = i32
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = i32
             _lib = lib
@@ -156,4 +159,29 @@ def sparse_mla_decode(q, kv_cache, page_table, topk_idx, softmax_scale,
         int(threads))
     if rc != 0:
         raise RuntimeError(f"oracle_sparse_mla_decode failed with status {rc}")
+    return out, lse
+
+
+def merge_states(o_a, lse_a, o_b, lse_b):
+    """LSE-weighted merge of two partial results over disjoint key sets.
+
+    o_*: [rows, d] float64 arrays (or bf16 torch tensors, widened exactly),
+    lse_*: [rows].  Returns (out [rows, d], lse [rows]) float64.
+    """
+    lib = _load()
+
+    def f64(x):
+        if not isinstance(x, np.ndarray):
+            x = x.detach().cpu().double().numpy()
+        return np.ascontiguousarray(x, dtype=np.float64)
+    oa, ob, la, lb = f64(o_a), f64(o_b), f64(lse_a).reshape(-1), f64(lse_b).reshape(-1)
+    rows = la.shape[0]
+    oa, ob = oa.reshape(rows, -1), ob.reshape(rows, -1)
+    d = oa.shape[1]
+    out = np.zeros((rows, d), dtype=np.float64)
+    lse = np.zeros((rows,), dtype=np.float64)
+    rc = lib.oracle_merge_states(_ptr(oa), _ptr(la), _ptr(ob), _ptr(lb), rows, d,
+                                 _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise RuntimeError(f"oracle_merge_states failed with status {rc}")
     return out, lse

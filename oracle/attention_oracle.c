@@ -286,6 +286,41 @@ int oracle_sparse_mla_decode(const uint16_t *q, const uint16_t *kv_cache,
     return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
 }
 
+/*
+ * Merge of two partial attention results of the same query rows over
+ * disjoint key sets A and B, weighted by their log-sum-exps:
+ *   L = ln(e^{L_A} + e^{L_B}),   O = e^{L_A - L} O_A + e^{L_B - L} O_B.
+ * An LSE of -inf marks an empty part (weight 0); both empty gives O = 0 and
+ * L = -inf.  Source: merge_attn_states on the vLLM page
+ * "vllm.v1.attention.backends.mla.prefill.flash_attn" (the context-chunk
+ * partial, non-causal with LSE, and the new-token partial, causal, are merged
+ * by their LSEs; FlashAttnPrefillBackend).
+ *   o_a, o_b: [rows, d]; lse_a, lse_b: [rows]; out: [rows, d]; lse: [rows].
+ */
+int oracle_merge_states(const double *o_a, const double *lse_a,
+                        const double *o_b, const double *lse_b, int64_t rows,
+                        int d, double *out, double *lse)
+{
+    if (!o_a || !lse_a || !o_b || !lse_b || !out || !lse || rows < 0 || d < 1)
+        return ORACLE_BAD_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        double la = lse_a[r], lb = lse_b[r];
+        double m = la > lb ? la : lb;
+        if (m == -INFINITY) {
+            for (int c = 0; c < d; ++c) out[(size_t)r * d + c] = 0.0;
+            lse[r] = -INFINITY;
+            continue;
+        }
+        double L = m + log(exp(la - m) + exp(lb - m));
+        double wa = exp(la - L), wb = exp(lb - L);
+        for (int c = 0; c < d; ++c)
+            out[(size_t)r * d + c] =
+                wa * o_a[(size_t)r * d + c] + wb * o_b[(size_t)r * d + c];
+        lse[r] = L;
+    }
+    return ORACLE_OK;
+}
+
 /* Number of OpenMP threads a parallel region would use. */
 int oracle_num_threads(void)
 {

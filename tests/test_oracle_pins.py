@@ -362,3 +362,40 @@ def test_decode_skips_out_of_range_slots():
     got, lgot = oracle.sparse_mla_decode(q, cache, page_table, bad, 0.1)
     np.testing.assert_array_equal(got, ref)
     np.testing.assert_array_equal(lgot, lref)
+
+
+# ------------------------------------------------------------ merge
+def test_merge_of_context_and_new_tokens_equals_full_chunked_prefill():
+    """Chunked prefill split: non-causal attention over the context keys,
+    causal attention over the new tokens' own keys, merged by LSE, equals
+    bottom-right causal attention over context + new keys (a decomposition
+    identity; the oracle's full run is itself pinned to SDPA above)."""
+    Lc, Ln, H, d = 37, 21, 3, 16
+    q = randn_bf16((Ln, H, d), 80)
+    kc, vc = randn_bf16((Lc, H, d), 81), randn_bf16((Lc, H, d), 82)
+    kn, vn = randn_bf16((Ln, H, d), 83), randn_bf16((Ln, H, d), 84)
+    scale = 0.3
+    o_ctx, l_ctx = oracle.varlen_attention(q, kc, vc, cu([Ln]), cu([Lc]), scale, causal=False)
+    o_new, l_new = oracle.varlen_attention(q, kn, vn, cu([Ln]), cu([Ln]), scale, causal=True)
+    merged, lm = oracle.merge_states(o_ctx, l_ctx, o_new, l_new)
+    k_all, v_all = torch.cat([kc, kn]), torch.cat([vc, vn])
+    full, lf = oracle.varlen_attention(q, k_all, v_all, cu([Ln]), cu([Lc + Ln]), scale,
+                                       causal=True)
+    np.testing.assert_allclose(merged, full, atol=1e-13)
+    np.testing.assert_allclose(lm, lf, atol=1e-13)
+
+
+def test_merge_with_empty_parts():
+    rng = np.random.default_rng(0)
+    o = rng.normal(size=(4, 8))
+    lse = np.array([0.3, -1.0, 2.0, 5.0])
+    empty_o, empty_l = np.zeros((4, 8)), np.full(4, -np.inf)
+    a, la = oracle.merge_states(o, lse, empty_o, empty_l)
+    np.testing.assert_array_equal(a, o)
+    np.testing.assert_array_equal(la, lse)
+    b, lb = oracle.merge_states(empty_o, empty_l, empty_o, empty_l)
+    np.testing.assert_array_equal(b, 0.0)
+    assert np.all(np.isneginf(lb))
+    c, lc = oracle.merge_states(o, lse, o, lse)     # equal halves: same O, LSE + ln 2
+    np.testing.assert_allclose(c, o, atol=1e-15)
+    np.testing.assert_allclose(lc, lse + math.log(2.0), atol=1e-15)
