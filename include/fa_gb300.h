@@ -138,6 +138,28 @@ fa_status fa_sparse_mla_decode(const void* q, const void* kv_cache,
                                fa_stream_t stream);
 
 /*
+ * fa_merge_attn_states -- merges two partial attention results of the same
+ * query rows computed over disjoint key sets, weighted by their LSEs:
+ *     L = ln(e^{L_prefix} + e^{L_suffix}),
+ *     O = e^{L_prefix - L} O_prefix + e^{L_suffix - L} O_suffix.
+ * Defined by [flash_attn] (merge_attn_states, used by FlashAttnPrefillBackend
+ * to combine the non-causal context-chunk partial with the causal
+ * new-token partial; both come from fa_varlen_fwd with an lse buffer).
+ *
+ *   out, prefix_out, suffix_out   bf16 [total_q, num_heads, head_dim]
+ *   out_lse (nullable), prefix_lse, suffix_lse   fp32 [num_heads, total_q]
+ *   head_dim      multiple of 8
+ * An LSE of -inf marks an empty part (weight 0); both empty gives O = 0 and
+ * LSE = -inf.  out may alias neither input.
+ * Host errors: FA_ERR_INVALID_ARG (null pointer, sizes, alignment),
+ * FA_ERR_UNSUPPORTED (more than 2^31 rows), FA_ERR_ARCH.
+ */
+fa_status fa_merge_attn_states(void* out, float* out_lse, const void* prefix_out,
+                               const float* prefix_lse, const void* suffix_out,
+                               const float* suffix_lse, int total_q, int num_heads,
+                               int head_dim, fa_stream_t stream);
+
+/*
  * fa_get_device_status -- reads and clears the library's device status word
  * on the current device.  Synchronises the device (not for the hot path).
  * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT if a kernel abandoned a pipeline wait

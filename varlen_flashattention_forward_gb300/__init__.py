@@ -13,6 +13,8 @@ Entry points (same names as the C ABI):
                 stream=None)
   fa_sparse_mla_decode(q, kv_cache, page_table, topk_idx, softmax_scale,
                        out=None, lse=None, return_lse=False, stream=None)
+  fa_merge_attn_states(prefix_out, prefix_lse, suffix_out, suffix_lse,
+                       out=None, out_lse=None, stream=None)
   fa_get_device_status()
 """
 from __future__ import annotations
@@ -31,8 +33,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
 
 # Exported C symbols (kept in sync with include/fa_gb300.h; a CPU test checks).
-EXPORTS = ("fa_varlen_fwd", "fa_sparse_mla_decode", "fa_get_device_status",
-           "fa_status_string")
+EXPORTS = ("fa_varlen_fwd", "fa_sparse_mla_decode", "fa_merge_attn_states",
+           "fa_get_device_status", "fa_status_string")
 
 _lib = None
 
@@ -60,6 +62,8 @@ def load_library():
     lib.fa_sparse_mla_decode.argtypes = [p, p, p, p, i32, i32, i32, i32, i32,
                                          f32, p, p, p]
     lib.fa_sparse_mla_decode.restype = i32
+    lib.fa_merge_attn_states.argtypes = [p, p, p, p, p, p, i32, i32, i32, p]
+    lib.fa_merge_attn_states.restype = i32
     lib.fa_get_device_status.argtypes = []
     lib.fa_get_device_status.restype = i32
     lib.fa_status_string.argtypes = [i32]
@@ -176,6 +180,34 @@ def fa_sparse_mla_decode(q, kv_cache, page_table, topk_idx, softmax_scale=None,
     if st != FA_OK:
         raise FaError(st, "fa_sparse_mla_decode")
     return (out, lse) if lse is not None else out
+
+
+def fa_merge_attn_states(prefix_out, prefix_lse, suffix_out, suffix_lse, out=None,
+                         out_lse=None, stream=None):
+    """LSE-weighted merge; see fa_merge_attn_states in include/fa_gb300.h.
+
+    *_out bf16 [T, H, d], *_lse fp32 [H, T] CUDA tensors.  Returns (out, out_lse).
+    """
+    import torch
+    lib = load_library()
+    for name, t in (("prefix_out", prefix_out), ("suffix_out", suffix_out)):
+        _check(t, name, torch.bfloat16, 3)
+    for name, t in (("prefix_lse", prefix_lse), ("suffix_lse", suffix_lse)):
+        _check(t, name, torch.float32, 2)
+    T, H, d = prefix_out.shape
+    if tuple(suffix_out.shape) != (T, H, d) or tuple(prefix_lse.shape) != (H, T) \
+            or tuple(suffix_lse.shape) != (H, T):
+        raise ValueError("merge inputs must be [T, H, d] outputs and [H, T] LSEs")
+    if out is None:
+        out = torch.empty_like(prefix_out)
+    if out_lse is None:
+        out_lse = torch.empty_like(prefix_lse)
+    st = lib.fa_merge_attn_states(_ptr(out), _ptr(out_lse), _ptr(prefix_out), _ptr(prefix_lse),
+                                  _ptr(suffix_out), _ptr(suffix_lse), T, H, d,
+                                  _stream_ptr(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_merge_attn_states")
+    return out, out_lse
 
 
 def fa_get_device_status() -> int:

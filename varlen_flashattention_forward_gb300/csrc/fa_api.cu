@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/fa_gb300.h"
+#include "merge_kernel.cuh"
 #include "sparse_decode_kernel.cuh"
 #include "varlen_fwd_kernel.cuh"
 
@@ -255,6 +256,34 @@ extern "C" fa_status fa_sparse_mla_decode(const void* q, const void* kv_cache,
   cudaError_t e = np == 64 ? fa::launch_decode_np<64>(qmap, a, st_)
                 : np == 32 ? fa::launch_decode_np<32>(qmap, a, st_)
                            : fa::launch_decode_np<16>(qmap, a, st_);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+extern "C" fa_status fa_merge_attn_states(void* out, float* out_lse, const void* prefix_out,
+                                          const float* prefix_lse, const void* suffix_out,
+                                          const float* suffix_lse, int total_q, int num_heads,
+                                          int head_dim, fa_stream_t stream) {
+  if (!out || !prefix_out || !prefix_lse || !suffix_out || !suffix_lse) return FA_ERR_INVALID_ARG;
+  if (total_q < 0 || num_heads < 1 || head_dim < 8 || head_dim % 8 != 0) return FA_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || !aligned(prefix_out, 16) || !aligned(suffix_out, 16) ||
+      !aligned(prefix_lse, 4) || !aligned(suffix_lse, 4) || (out_lse && !aligned(out_lse, 4)))
+    return FA_ERR_INVALID_ARG;
+  if ((int64_t)total_q * num_heads > INT32_MAX) return FA_ERR_UNSUPPORTED;
+  DeviceInfo* dev = nullptr;
+  fa_status st = device_info(&dev);
+  if (st != FA_OK) return st;
+  if (total_q == 0) return FA_OK;
+  fa::MergeArgs a;
+  a.oa = static_cast<const uint16_t*>(prefix_out);
+  a.la = prefix_lse;
+  a.ob = static_cast<const uint16_t*>(suffix_out);
+  a.lb = suffix_lse;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = out_lse;
+  a.total_q = total_q;
+  a.num_heads = num_heads;
+  a.head_dim = head_dim;
+  cudaError_t e = fa::launch_merge(a, dev->sm_count, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
