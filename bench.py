@@ -277,22 +277,112 @@ def extra_lines(steps, warmup, device, peaks):
     return res
 
 
+def decode_oracle_rate(d, budget_s, seed=0):
+    """fp64 oracle on a random sample of (token, head) rows of the decode
+    workload (small cache: only the sampled tokens' pages are drawn)."""
+    import oracle
+    pt, ti = d.make_indices()
+    q = d.make_q()
+    rng = np.random.default_rng(seed)
+    # Only the pages the sampled tokens reference are materialised; the
+    # others are never read by the oracle.
+    def run(n_tok):
+        toks = np.sort(rng.choice(d.num_tokens, size=n_tok, replace=False))
+        pages = pt[toks].reshape(-1).long()
+        g = torch.Generator().manual_seed(seed)
+        small = workloads._randn((pages.numel(), d.page_size, 576), g, 1.0)
+        remap = torch.arange(pages.numel(), dtype=torch.int32).view(n_tok, -1)
+        t0 = time.perf_counter()
+        oracle.sparse_mla_decode(q[toks].contiguous(), small, remap, ti[toks].contiguous(),
+                                 d.softmax_scale)
+        dt = time.perf_counter() - t0
+        return n_tok * d.topk * 576 * 2.0, dt, n_tok
+    byts, dt, n = run(1)
+    n2 = max(1, min(d.num_tokens, int(budget_s / max(dt, 1e-3))))
+    byts, dt, n = run(n2)
+    return byts / dt, n, dt, oracle.num_threads()
+
+
+def main_decode(a, world, rank, local, peaks):
+    """Sparse-MLA decode line: bound by HBM bandwidth."""
+    d = workloads.DecodeWorkload()
+    if a.decode_tokens:
+        # Smaller case (profiling): same per-token shape, fewer tokens/pages.
+        d = workloads.DecodeWorkload(num_tokens=a.decode_tokens,
+                                     num_pages=a.decode_tokens * d.pages_per_token)
+    byts = metrics.decode_alg_bytes(d)
+    config = {"workload": "sparse_mla_decode", "num_tokens": d.num_tokens,
+              "num_heads": d.num_heads, "topk": d.topk, "context": d.context,
+              "num_pages": d.num_pages, "page_size": d.page_size,
+              "l2": "flushed before every timed step (512 MB write)",
+              "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    if a.impl == "reference":
+        if rank != 0:
+            return
+        rates = [decode_oracle_rate(d, a.cpu_budget / 4, seed=s)
+                 for s in range(a.warmup + a.steps)][a.warmup:]
+        val = statistics.mean(r[0] for r in rates) / 1e9
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": 1,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": byts / (val * 1e9) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config,
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": rates[0][3], "kind": "oracle",
+                             "sample": f"{rates[0][1]} tokens per step, fp64 oracle"},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}))
+        return
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import varlen_flashattention_forward_gb300 as fa
+    fa.load_library()
+    with ClockSampler(local) as clk:
+        times = time_decode(d, a.steps, a.warmup, device)
+    ms = max_over_ranks(statistics.mean(times), world)
+    if rank != 0:
+        return
+    gbs = byts / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(gbs * world, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config,
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                     "peak_source": peaks["source"] + " HBM copy",
+                     "kernel": "sparse_decode_kernel<64>", "alg_bytes_per_launch": byts,
+                     "alg_flops_per_launch": metrics.decode_flops(d)},
+        "tflops": round(metrics.decode_flops(d) / (ms * 1e-3) / 1e12, 1),
+        "gpu_launches": a.steps, "clocks": clk.summary(),
+    }
+    if not a.no_cpu_baseline:
+        rate, n, dt, threads = decode_oracle_rate(d, a.cpu_budget)
+        line["cpu_baseline"] = {"value": rate / 1e9, "unit": "GB/s", "cores": threads,
+                                "kind": "oracle", "sample": f"{n} tokens, {dt:.1f} s, fp64"}
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="vit_full_d80")
+    ap.add_argument("--workload", default="vit_full_d80",
+                    help="a varlen workload name or 'decode'")
     ap.add_argument("--extra", action="store_true", help="also time the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-tokens", type=int, default=0,
+                    help="decode workload with this many tokens (default: 128)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
 
     world, rank, local = dist_setup()
-    w = workloads.VARLEN_BENCH[a.workload]()
     peaks = load_peaks()
+    if a.workload == "decode":
+        return main_decode(a, world, rank, local, peaks)
+    w = workloads.VARLEN_BENCH[a.workload]()
     flops = metrics.varlen_flops(w)
     byts = metrics.varlen_alg_bytes(w)
     config = {"workload": w.name, "lens": w.lens_q, "num_heads": w.num_heads,

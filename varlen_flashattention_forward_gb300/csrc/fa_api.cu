@@ -163,14 +163,13 @@ extern "C" fa_status fa_varlen_fwd(const void* q, const void* k, const void* v,
   const int kh = total_k > 0 ? num_heads_k : num_heads;
   const int vd = total_k > 0 ? d_v : d_qk;
   const int tk = total_k > 0 ? total_k : total_q;
-  const int qt = tail_width(d_qk), vt = tail_width(d_v);
+  const int qt = tail_width(d_qk);
   bool ok = encode_rows(&maps.q_full, q, d_qk, num_heads, total_q, 64, fa::kBM) &&
             encode_rows(&maps.k_full, kb, d_qk, kh, tk, 64, fa::kBN) &&
             encode_rows(&maps.v_full, vb, vd, kh, tk, 64, fa::kBN);
   if (ok && qt)
     ok = encode_rows(&maps.q_tail, q, d_qk, num_heads, total_q, qt, fa::kBM) &&
          encode_rows(&maps.k_tail, kb, d_qk, kh, tk, qt, fa::kBN);
-  if (ok && vt) ok = encode_rows(&maps.v_tail, vb, vd, kh, tk, vt, fa::kBN);
   if (!ok) return FA_ERR_LAUNCH;
 
   fa::VarlenArgs args;

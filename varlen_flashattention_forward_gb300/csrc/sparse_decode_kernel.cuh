@@ -11,7 +11,11 @@
 //   producer warps 4-7  gather 64 rows per tile with 16-byte cp.async into a
 //                       2-stage ring (128-byte swizzle, the UMMA K-major layout
 //                       for Sᵀ and the MN-major layout for Oᵀ);
-//   MMA warp 8          TMA-loads Q once, issues both MMAs (one thread);
+//   MMA warp 8          TMA-loads Q once and issues Sᵀ as soon as a tile has
+//                       landed and its Sᵀ buffer is free;
+//   MMA warp 9          issues Oᵀ += Rᵀ·Pᵀ as soon as Pᵀ is ready and
+//                       releases the stage (two issuers, so waiting for the
+//                       next gathered tile never delays the current PV);
 //   softmax warps 0-3   one thread per key of the tile: per-head maximum over
 //                       the tile's keys (shuffle transpose-reduce + shared
 //                       memory), exp2 with a lazily rescaled running maximum,
@@ -38,7 +42,7 @@
 namespace fa {
 
 constexpr int kDecodePage = 64;
-constexpr int kDecodeThreads = 384;   // softmax 0-3, producers 4-7, MMA 8, idle 9-11
+constexpr int kDecodeThreads = 384;   // softmax 0-3, gather 4-7, S issuer 8, PV issuer 9, idle 10-11
 // Register split (launch: 168 x 384 = 64512): softmax 128 x 240, gather
 // 128 x 88, control 128 x 56 = 49152.
 constexpr uint32_t kDecodeSoftmaxRegs = 240;
@@ -69,6 +73,7 @@ struct alignas(8) DecodeCtl {
   uint64_t r_full[2];
   uint64_t r_free[2];
   uint64_t s_full[2];
+  uint64_t s_free[2];
   uint64_t p_full;
   uint64_t pv_done;
   uint64_t drain;
@@ -176,10 +181,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       ptx::mbar_init(ptx::smem_u32(&cb->r_full[s]), 128);
       ptx::mbar_init(ptx::smem_u32(&cb->r_free[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&cb->s_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&cb->s_free[s]), 128);
     }
     ptx::mbar_init(ptx::smem_u32(&cb->p_full), 128);
     ptx::mbar_init(ptx::smem_u32(&cb->pv_done), 1);
-    ptx::mbar_init(ptx::smem_u32(&cb->drain), 1);
+    ptx::mbar_init(ptx::smem_u32(&cb->drain), 2);
     cb->abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -241,66 +247,63 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     cp_async_wait<0>();  // nothing of this thread is in flight at exit
   } else if (warp >= 8) {
     ptx::regs_dec<kDecodeControlRegs>();
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ MMA issuers
+    constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(64, NP, false, false);
+    constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(128, NP, true, true);
     if (warp == 8 && lane == 0) {
-      constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(64, NP, false, false);
-      constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(128, NP, true, true);
+      // Sᵀ(j) = R(j) Qᵀ into Sᵀ buffer j % 2.
       ptx::prefetch_tmap(&q_map);
       ptx::mbar_arrive_expect_tx(ptx::smem_u32(&cb->q_full), 9 * NP * 128);
       for (int c = 0; c < 9; ++c)
         ptx::tma_load_3d(ptx::smem_u32(q_s + c * NP * 128), &q_map, ptx::smem_u32(&cb->q_full),
                          c * 64, head0, token);
       bool ok = wait_single(ptx::smem_u32(&cb->q_full), 0, abort_flag, a.status);
-      const uint32_t qa = ptx::smem_u32(q_s);
-      auto issue_s = [&](int j) {
-        const uint32_t ra = ptx::smem_u32(stage[j & 1]);
-        const uint32_t d = tmem + (uint32_t)((j & 1) * NP);
-#pragma unroll
-        for (int k = 0; k < kDqk / 16; ++k) {
-          const int c = k >> 2;
-          const uint32_t in = (k & 3) * 32;
-          const uint64_t ad = ptx::smem_desc(ra + c * kChunkBytes + in, 16, 1024, ptx::kLayoutSw128);
-          const uint64_t bd = ptx::smem_desc(qa + c * NP * 128 + in, 16, 1024, ptx::kLayoutSw128);
-          ptx::mma_ss(d, ad, bd, idesc_s, k > 0 ? 1u : 0u);
-        }
-      };
-      if (ok) ok = wait_single(ptx::smem_u32(&cb->r_full[0]), 0, abort_flag, a.status);
-      if (ok) {
+      const uint64_t qd = ptx::smem_desc(ptx::smem_u32(q_s), 16, 1024, ptx::kLayoutSw128);
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        ok = wait_single(ptx::smem_u32(&cb->r_full[j & 1]), (j >> 1) & 1, abort_flag, a.status);
+        if (ok && j >= 2)
+          ok = wait_single(ptx::smem_u32(&cb->s_free[j & 1]), ((j >> 1) - 1) & 1, abort_flag,
+                           a.status);
+        if (!ok) break;
         // The gathered rows were written by cp.async (generic proxy); order
         // them before the tensor core's (async proxy) reads.
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_after();
-        issue_s(0);
-        ptx::mma_commit(ptx::smem_u32(&cb->s_full[0]));
-      }
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        if (j + 1 < n_tiles) {
-          ok = wait_single(ptx::smem_u32(&cb->r_full[(j + 1) & 1]), ((j + 1) >> 1) & 1, abort_flag,
-                           a.status);
-          if (!ok) break;
-          ptx::fence_proxy_async_smem();
-          ptx::tc_fence_after();
-          issue_s(j + 1);
-          ptx::mma_commit(ptx::smem_u32(&cb->s_full[(j + 1) & 1]));
+        const uint64_t rd =
+            ptx::smem_desc(ptx::smem_u32(stage[j & 1]), 16, 1024, ptx::kLayoutSw128);
+        const uint32_t d = tmem + (uint32_t)((j & 1) * NP);
+#pragma unroll
+        for (int k = 0; k < kDqk / 16; ++k) {
+          const uint32_t in = (k & 3) * 32;
+          ptx::mma_ss(d, ptx::desc_add(rd, (k >> 2) * kChunkBytes + in),
+                      ptx::desc_add(qd, (k >> 2) * NP * 128 + in), idesc_s, k > 0 ? 1u : 0u);
         }
+        ptx::mma_commit(ptx::smem_u32(&cb->s_full[j & 1]));
+      }
+      ptx::mma_commit(ptx::smem_u32(&cb->drain));
+      wait_single(ptx::smem_u32(&cb->drain), 0, abort_flag, a.status);
+    } else if (warp == 9 && lane == 0) {
+      // Oᵀ += R(j)[:, 0:512]ᵀ Pᵀ(j), then release stage j % 2.
+      bool ok = true;
+      for (int j = 0; j < n_tiles && ok; ++j) {
         ok = wait_single(ptx::smem_u32(&cb->p_full), j & 1, abort_flag, a.status);
         if (!ok) break;
+        ptx::fence_proxy_async_smem();
         ptx::tc_fence_after();
         const uint32_t ra = ptx::smem_u32(stage[j & 1]);
-        const uint32_t pa = ra + 8 * kChunkBytes;  // Pᵀ lives in the rope chunk
+        // A = R[keys, 128m .. 128m+128)ᵀ: MN-major, two 64-wide chunks.
+        const uint64_t ad = ptx::smem_desc(ra, kChunkBytes, 1024, ptx::kLayoutSw128);
+        // B = Pᵀ[keys, heads] in the rope chunk: MN-major, NP wide.
+        const uint64_t bd =
+            ptx::smem_desc(ra + 8 * kChunkBytes, 8 * kPRowBytes, 8 * kPRowBytes, kSwP);
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-          const uint32_t d = tmem + 128u + (uint32_t)(m * NP);
 #pragma unroll
-          for (int k = 0; k < kDecodeKeys / 16; ++k) {
-            // A = R[keys, 128m .. 128m+128)ᵀ: MN-major, two 64-wide chunks.
-            const uint64_t ad = ptx::smem_desc(ra + 2 * m * kChunkBytes + k * 16 * 128,
-                                               kChunkBytes, 1024, ptx::kLayoutSw128);
-            // B = Pᵀ[keys, heads]: MN-major, NP wide (one swizzle atom).
-            const uint64_t bd = ptx::smem_desc(pa + k * 16 * kPRowBytes, 8 * kPRowBytes,
-                                               8 * kPRowBytes, kSwP);
-            ptx::mma_ss(d, ad, bd, idesc_o, (j > 0 || k > 0) ? 1u : 0u);
-          }
+          for (int k = 0; k < kDecodeKeys / 16; ++k)
+            ptx::mma_ss(tmem + 128u + (uint32_t)(m * NP),
+                        ptx::desc_add(ad, 2 * m * kChunkBytes + k * 16 * 128),
+                        ptx::desc_add(bd, k * 16 * kPRowBytes), idesc_o,
+                        (j > 0 || k > 0) ? 1u : 0u);
         }
         ptx::mma_commit(ptx::smem_u32(&cb->pv_done));
         ptx::mma_commit(ptx::smem_u32(&cb->r_free[j & 1]));
@@ -336,6 +339,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       ptx::tmem_wait_ld();
 #pragma unroll
       for (int c = 0; c < NP; c += 16) ptx::reg_fence16(sr + c);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_u32(&cb->s_free[j & 1]));  // Sᵀ buffer may be reused
       const bool valid = holds_key && rows[j * kDecodeKeys + key_in_tile] >= 0;
       float s[NP], v[NP];
 #pragma unroll

@@ -5,9 +5,16 @@
 //
 //   producer warp   TMA: Q tiles once, then K_j, V_j tiles into a ring of
 //                   shared-memory slots guarded by mbarriers.
-//   MMA warp        tcgen05.mma (one elected thread):
+//   MMA warps 9/10  one elected thread per query tile t issues tcgen05.mma:
 //                     S_t = Q_t K_jᵀ          (SS form, fp32 accumulator in TMEM)
 //                     O_t += P_t V_j          (TS form, P read from TMEM)
+//                   Two issuers keep the two tiles' chains independent: a
+//                   thread blocked on a full tensor-core queue while issuing
+//                   one tile's MMAs cannot delay the other tile.  They take
+//                   turns per issue group (tile 0 group g, tile 1 group g,
+//                   tile 0 group g+1, ...) so the tensor core alternates
+//                   between the tiles and each tile's softmax runs while the
+//                   other tile's MMAs execute (ping-pong).
 //   softmax WG t    one thread per query row (TMEM lane): loads S_t, masks only
 //                   boundary tiles, 3-input max reduction, exp2, row sum,
 //                   lazy O rescale (threshold kRescaleLog2), writes P_t as bf16
@@ -41,9 +48,9 @@
 
 namespace fa {
 
-constexpr int kVarlenThreads = 384;   // 2 softmax warpgroups + {producer, MMA, 2 idle} warps
+constexpr int kVarlenThreads = 384;   // 2 softmax warpgroups + {producer, 2 MMA, 1 idle} warps
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;           // issuer of tile 0 (and TMEM owner); warp 10 issues tile 1
 // Register split (launch: 168 per thread x 384 threads = 64512):
 // softmax warpgroups 2 x 128 x 208 + control warpgroup 128 x 56 = 60416.
 constexpr uint32_t kSoftmaxRegs = 208;
@@ -82,7 +89,11 @@ struct VarlenCfg {
   using VD = HeadDim<D_V>;
   static constexpr int q_tile_bytes = QK::tile_bytes(kBM);
   static constexpr int k_tile_bytes = QK::tile_bytes(kBN);
-  static constexpr int v_tile_bytes = VD::tile_bytes(kBN);
+  // V is stored as whole 64-wide swizzle atoms (TMA zero-fills columns past
+  // d_v), so that P V is one N = d_v MMA per 16 keys: a tensor-core
+  // instruction costs about the same for any N up to 128.
+  static constexpr int v_chunks = (VD::padded + 63) / 64;
+  static constexpr int v_tile_bytes = v_chunks * kBN * 128;
   static constexpr int slot_bytes =
       ((k_tile_bytes > v_tile_bytes ? k_tile_bytes : v_tile_bytes) + 1023) / 1024 * 1024;
   static constexpr int sched_bytes_max = 8 * (kMaxBatch + 1) + 4 * kVarlenThreads;
@@ -112,18 +123,19 @@ struct VarlenArgs {
 };
 
 struct VarlenMaps {
-  CUtensorMap q_full, q_tail, k_full, k_tail, v_full, v_tail;
+  CUtensorMap q_full, q_tail, k_full, k_tail, v_full;
 };
 
 // Shared-memory control block (after the tiles).
 struct alignas(8) VarlenBarriers {
   uint64_t q_full[2];
-  uint64_t q_free;
+  uint64_t q_free[2];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_full[2];
   uint64_t o_free[2];
   uint64_t drain;
+  uint64_t turn[2];  // issuer t may issue its next group
   uint64_t kv_full[8];
   uint64_t kv_free[8];
   uint32_t tmem_base;
@@ -319,11 +331,14 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
       ptx::mbar_init(ptx::smem_u32(&cb->o_full[t]), 1);
       ptx::mbar_init(ptx::smem_u32(&cb->o_free[t]), kBM);
     }
-    ptx::mbar_init(ptx::smem_u32(&cb->q_free), 1);
-    ptx::mbar_init(ptx::smem_u32(&cb->drain), 1);
+    ptx::mbar_init(ptx::smem_u32(&cb->q_free[0]), 1);
+    ptx::mbar_init(ptx::smem_u32(&cb->q_free[1]), 1);
+    ptx::mbar_init(ptx::smem_u32(&cb->drain), 2);
+    ptx::mbar_init(ptx::smem_u32(&cb->turn[0]), 1);
+    ptx::mbar_init(ptx::smem_u32(&cb->turn[1]), 1);
     for (int s = 0; s < NS; ++s) {
       ptx::mbar_init(ptx::smem_u32(&cb->kv_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&cb->kv_free[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&cb->kv_free[s]), 2);  // one release per issuer
     }
     cb->abort_flag = 0;
     ptx::fence_mbar_init();
@@ -336,7 +351,6 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
       ptx::prefetch_tmap(&maps.q_tail);
       ptx::prefetch_tmap(&maps.k_tail);
     }
-    if (VD::tail) ptx::prefetch_tmap(&maps.v_tail);
   }
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(&cb->tmem_base), 512);
@@ -354,7 +368,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     if (warp == kProducerWarp) {
       // ---------------------------------------------------------- producer
       if (lane == 0) {
-        uint32_t qf_n = 0;
+        uint32_t qf_n[2] = {0, 0};
         int slot = 0;
         uint32_t phase = 0;
         uint32_t q_issued[2] = {0, 0};
@@ -363,10 +377,11 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         for (int it = blockIdx.x; it < total_items && ok; it += gridDim.x) {
           const WorkItem w = decode_item(it, args, s_prefix, s_sorted);
           if (w.n_kv == 0) continue;
-          ok = wait_single(ptx::smem_u32(&cb->q_free), (qf_n & 1) ^ 1, abort_flag, args.status);
-          ++qf_n;
-          if (!ok) break;
-          for (int t = 0; t < w.n_qt; ++t) {
+          for (int t = 0; t < w.n_qt && ok; ++t) {
+            ok = wait_single(ptx::smem_u32(&cb->q_free[t]), (qf_n[t] & 1) ^ 1, abort_flag,
+                             args.status);
+            ++qf_n[t];
+            if (!ok) break;
             const uint32_t bar = ptx::smem_u32(&cb->q_full[t]);
             ptx::mbar_arrive_expect_tx(bar, C::q_tile_bytes);
             ++q_issued[t];
@@ -395,9 +410,8 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
               } else {
                 ptx::mbar_arrive_expect_tx(bar, C::v_tile_bytes);
 #pragma unroll
-                for (int c = 0; c < VD::chunks; ++c)
-                  ptx::tma_load_3d(ptx::smem_u32(dst + VD::chunk_off(c, kBN)),
-                                   c < VD::full ? &maps.v_full : &maps.v_tail, bar, c * 64,
+                for (int c = 0; c < C::v_chunks; ++c)
+                  ptx::tma_load_3d(ptx::smem_u32(dst + c * kBN * 128), &maps.v_full, bar, c * 64,
                                    w.kv_head, krow);
               }
               ++slot_issued[slot];
@@ -418,14 +432,23 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         }
       }
       __syncwarp();
-    } else if (warp == kMmaWarp) {
-      // ---------------------------------------------------------- MMA issuer
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+      // ---------------------------------------------------------- MMA issuers
       if (lane == 0) {
+        const int t = warp - kMmaWarp;  // query tile this thread issues for
         constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(kBM, kBN, false, false);
-        constexpr uint32_t idesc_pv_full = ptx::idesc_bf16_f32(kBM, 64, false, true);
-        constexpr uint32_t idesc_pv_tail =
-            ptx::idesc_bf16_f32(kBM, VD::tail ? VD::tail : 16, false, true);
-        uint32_t qn[2] = {0, 0}, pn[2] = {0, 0}, ofn[2] = {0, 0};
+        uint32_t qn = 0, pn = 0, ofn = 0;
+        uint32_t groups = 0;  // issue groups done by this issuer
+        // Wait for this issuer's turn; issuer 0 starts.
+        auto take_turn = [&]() -> bool {
+          if (t == 0 && groups == 0) return true;
+          const uint32_t par = (t == 0 ? groups - 1 : groups) & 1;
+          return wait_single(ptx::smem_u32(&cb->turn[t]), par, abort_flag, args.status);
+        };
+        auto pass_turn = [&]() {
+          ptx::mbar_arrive(ptx::smem_u32(&cb->turn[t ^ 1]));
+          ++groups;
+        };
         int slot = 0;
         uint32_t phase = 0;
         bool ok = true;
@@ -437,8 +460,6 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         // instruction count matters).
         constexpr uint32_t kQkTailSbo = 8 * (QK::tail ? QK::tail : 16) * 2;
         constexpr uint32_t kQkTailLay = layout_for_width(QK::tail ? QK::tail : 16);
-        constexpr uint32_t kVTailSbo = 8 * (VD::tail ? VD::tail : 16) * 2;
-        constexpr uint32_t kVTailLay = layout_for_width(VD::tail ? VD::tail : 16);
         uint64_t q_desc[2], q_desc_tail[2];
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -447,7 +468,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           q_desc_tail[t] =
               ptx::smem_desc(qa + QK::chunk_off(QK::full, kBM), 16, kQkTailSbo, kQkTailLay);
         }
-        auto issue_s = [&](int t, const uint8_t* kbuf) {
+        auto issue_s = [&](const uint8_t* kbuf) {
           const uint32_t d = tmem + C::s_col(t);
           const uint32_t ka = ptx::smem_u32(kbuf);
           const uint64_t kd = ptx::smem_desc(ka, 16, 1024, ptx::kLayoutSw128);
@@ -468,112 +489,90 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             }
           }
         };
-        auto issue_pv = [&](int t, const uint8_t* vbuf, bool first) {
-          const uint32_t va = ptx::smem_u32(vbuf);
+        auto issue_pv = [&](const uint8_t* vbuf, bool first) {
+          // One MMA per 16 keys over all of d_v: MN-major B spanning
+          // C::v_chunks 64-wide atoms, kBN * 128 bytes apart.
+          constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(kBM, VD::padded, false, true);
+          const uint64_t vd =
+              ptx::smem_desc(ptx::smem_u32(vbuf), kBN * 128, 1024, ptx::kLayoutSw128);
           const uint32_t a0 = tmem + C::s_col(t);
-          if (VD::tail == 0) {
-            // One MMA per 16 keys over all of d_v: MN-major B spanning
-            // VD::full 64-wide atoms, VD::chunk_off(1, kBN) bytes apart.
-            constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(kBM, VD::padded, false, true);
-            const uint64_t vd =
-                ptx::smem_desc(va, VD::chunk_off(1, kBN), 1024, ptx::kLayoutSw128);
 #pragma unroll
-            for (int s = 0; s < kBN / 16; ++s)
-              ptx::mma_ts(tmem + C::o_col(t), a0 + s * 8, ptx::desc_add(vd, s * 16 * 128),
-                          idesc_pv, (!first || s > 0) ? 1u : 0u);
-          } else {
-            // A 64-wide chunk (or none) plus a narrower tail chunk with its own
-            // swizzle.  For the MN extent inside one atom only the 8-key-group
-            // stride matters; it is given in both offset fields.
-            const uint64_t vd = ptx::smem_desc(va, 1024, 1024, ptx::kLayoutSw128);
-            const uint64_t vd_tail =
-                ptx::smem_desc(va + VD::chunk_off(VD::full, kBN), kVTailSbo, kVTailSbo, kVTailLay);
-#pragma unroll
-            for (int s = 0; s < kBN / 16; ++s) {
-#pragma unroll
-              for (int c = 0; c < VD::full; ++c)
-                ptx::mma_ts(tmem + C::o_col(t) + c * 64, a0 + s * 8,
-                            ptx::desc_add(vd, VD::chunk_off(c, kBN) + s * 16 * 128),
-                            idesc_pv_full, (!first || s > 0) ? 1u : 0u);
-              ptx::mma_ts(tmem + C::o_col(t) + VD::full * 64, a0 + s * 8,
-                          ptx::desc_add(vd_tail, s * 16 * VD::tail * 2), idesc_pv_tail,
-                          (!first || s > 0) ? 1u : 0u);
-            }
-          }
+          for (int s = 0; s < kBN / 16; ++s)
+            ptx::mma_ts(tmem + C::o_col(t), a0 + s * 8, ptx::desc_add(vd, s * 16 * 128), idesc_pv,
+                        (!first || s > 0) ? 1u : 0u);
         };
-
+        // Both issuers walk every KV tile of every item (to stay in phase on
+        // the ring); an issuer whose tile is absent from the item only waits
+        // and releases.
         for (int it = blockIdx.x; it < total_items && ok; it += gridDim.x) {
           const WorkItem w = decode_item(it, args, s_prefix, s_sorted);
           if (w.n_kv == 0) continue;
-          issued_any = true;
-          const int nt = w.n_qt;
-          for (int t = 0; t < nt && ok; ++t) {
-            ok = wait_single(ptx::smem_u32(&cb->q_full[t]), qn[t] & 1, abort_flag, args.status);
-            ++qn[t];
+          const bool mine = t < w.n_qt;
+          if (mine) {
+            issued_any = true;
+            ok = wait_single(ptx::smem_u32(&cb->q_full[t]), qn & 1, abort_flag, args.status);
+            ++qn;
+            if (!ok) break;
           }
-          if (!ok) break;
-          // Prologue: S_t(0) for both tiles.
+          // Prologue: S_t(0).
           ok = wait_single(ptx::smem_u32(&cb->kv_full[slot]), phase, abort_flag, args.status);
+          if (ok) ok = take_turn();
           if (!ok) break;
           ptx::tc_fence_after();
-          {
-            const uint8_t* kbuf = ring + slot * C::slot_bytes;
-            for (int t = 0; t < nt; ++t) {
-              issue_s(t, kbuf);
-              ptx::mma_commit(ptx::smem_u32(&cb->s_full[t]));
-            }
-            ptx::mma_commit(ptx::smem_u32(&cb->kv_free[slot]));
-            if (w.n_kv == 1) ptx::mma_commit(ptx::smem_u32(&cb->q_free));
-            if (++slot == NS) { slot = 0; phase ^= 1; }
+          if (mine) {
+            issue_s(ring + slot * C::slot_bytes);
+            ptx::mma_commit(ptx::smem_u32(&cb->s_full[t]));
+            if (w.n_kv == 1) ptx::mma_commit(ptx::smem_u32(&cb->q_free[t]));
           }
+          ptx::mma_commit(ptx::smem_u32(&cb->kv_free[slot]));
+          pass_turn();
+          if (++slot == NS) { slot = 0; phase ^= 1; }
           for (int j = 0; j < w.n_kv && ok; ++j) {
             const int vslot = slot;
             ok = wait_single(ptx::smem_u32(&cb->kv_full[vslot]), phase, abort_flag, args.status);
             if (!ok) break;
             if (++slot == NS) { slot = 0; phase ^= 1; }
-            const uint8_t* vbuf = ring + vslot * C::slot_bytes;
             const bool has_next = j + 1 < w.n_kv;
-            int kslot = 0;
-            for (int t = 0; t < nt && ok; ++t) {
-              ok = wait_single(ptx::smem_u32(&cb->p_full[t]), pn[t] & 1, abort_flag, args.status);
-              ++pn[t];
+            ok = take_turn();
+            if (!ok) break;
+            if (mine) {
+              ok = wait_single(ptx::smem_u32(&cb->p_full[t]), pn & 1, abort_flag, args.status);
+              ++pn;
               if (!ok) break;
               if (j == 0) {
-                ok = wait_single(ptx::smem_u32(&cb->o_free[t]), (ofn[t] & 1) ^ 1, abort_flag,
+                ok = wait_single(ptx::smem_u32(&cb->o_free[t]), (ofn & 1) ^ 1, abort_flag,
                                  args.status);
-                ++ofn[t];
+                ++ofn;
                 if (!ok) break;
               }
               ptx::tc_fence_after();
-              issue_pv(t, vbuf, j == 0);
-              if (has_next) {
-                if (t == 0) {
-                  kslot = slot;
-                  ok = wait_single(ptx::smem_u32(&cb->kv_full[kslot]), phase, abort_flag,
-                                   args.status);
-                  if (!ok) break;
-                  if (++slot == NS) { slot = 0; phase ^= 1; }
-                  ptx::tc_fence_after();
-                }
-                issue_s(t, ring + kslot * C::slot_bytes);
-                ptx::mma_commit(ptx::smem_u32(&cb->s_full[t]));
-              } else {
-                ptx::mma_commit(ptx::smem_u32(&cb->o_full[t]));
-              }
+              issue_pv(ring + vslot * C::slot_bytes, j == 0);
             }
-            if (!ok) break;
             if (has_next) {
+              const int kslot = slot;
+              ok = wait_single(ptx::smem_u32(&cb->kv_full[kslot]), phase, abort_flag,
+                               args.status);
+              if (!ok) break;
+              if (++slot == NS) { slot = 0; phase ^= 1; }
+              if (mine) {
+                ptx::tc_fence_after();
+                issue_s(ring + kslot * C::slot_bytes);
+                ptx::mma_commit(ptx::smem_u32(&cb->s_full[t]));
+                if (j + 2 == w.n_kv) ptx::mma_commit(ptx::smem_u32(&cb->q_free[t]));
+              }
               ptx::mma_commit(ptx::smem_u32(&cb->kv_free[kslot]));
-              if (j + 2 == w.n_kv) ptx::mma_commit(ptx::smem_u32(&cb->q_free));
+            } else if (mine) {
+              ptx::mma_commit(ptx::smem_u32(&cb->o_full[t]));
             }
             ptx::mma_commit(ptx::smem_u32(&cb->kv_free[vslot]));
+            pass_turn();
           }
         }
-        if (issued_any) {
-          // Drain: every MMA issued by this thread completes before TMEM is freed.
-          ptx::mma_commit(ptx::smem_u32(&cb->drain));
-          wait_single(ptx::smem_u32(&cb->drain), 0, abort_flag, args.status);
-        }
+        // Drain: every MMA issued by either issuer completes before TMEM is
+        // freed (the barrier expects one arrival from each issuer).
+        (void)issued_any;
+        ptx::mma_commit(ptx::smem_u32(&cb->drain));
+        wait_single(ptx::smem_u32(&cb->drain), 0, abort_flag, args.status);
       }
       __syncwarp();
     }
@@ -662,16 +661,28 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           }
         }
         const float base = (m_used == neg_inf) ? 0.f : m_used;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        // exp2(s * scale_log2 - base) with packed fp32x2 FMA / ADD (one
+        // instruction per element pair), MUFU ex2 per element, and the row
+        // sum in four independent packed accumulators.
+        const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
+        const uint64_t nbx2 = ptx::f2_pack(-base, -base);
+        uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
         uint32_t pr[kBN / 2];
 #pragma unroll
         for (int c = 0; c < kBN; c += 2) {
-          const float p0 = ptx::ex2(fmaf(s[c], sl2, -base));
-          const float p1 = ptx::ex2(fmaf(s[c + 1], sl2, -base));
-          ls[(c >> 1) & 3] += p0 + p1;
+          float x0, x1;
+          ptx::f2_unpack(ptx::fma2(ptx::f2_pack(s[c], s[c + 1]), sl2x2, nbx2), x0, x1);
+          const float p0 = ptx::ex2(x0);
+          const float p1 = ptx::ex2(x1);
+          ls2[(c >> 1) & 3] = ptx::add2(ls2[(c >> 1) & 3], ptx::f2_pack(p0, p1));
           pr[c >> 1] = ptx::pack_bf16x2(p0, p1);
         }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        {
+          float a0, a1, b0, b1;
+          ptx::f2_unpack(ptx::add2(ls2[0], ls2[1]), a0, a1);
+          ptx::f2_unpack(ptx::add2(ls2[2], ls2[3]), b0, b1);
+          l += (a0 + b0) + (a1 + b1);
+        }
 #pragma unroll
         for (int q = 0; q < kBN / 2; q += 32) ptx::tmem_st32(s_addr + q, pr + q);
         ptx::tmem_wait_st();
