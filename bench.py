@@ -132,6 +132,12 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def whole_job_rate(units_per_rank: float, ms_max: float, world: int) -> float:
+    """Whole-job throughput of `world` replicas that each processed
+    `units_per_rank` units, timed by the slowest rank (ms_max): units per second."""
+    return units_per_rank * world / (ms_max * 1e-3)
+
+
 # ------------------------------------------------------------ CPU oracle timing
 def oracle_sample_rate(w, budget_s: float, seed: int = 0):
     """Times the fp64 oracle on a random sample of (token, head) rows of the
@@ -343,7 +349,8 @@ def main_decode(a, world, rank, local, peaks):
         return
     gbs = byts / (ms * 1e-3) / 1e9
     line = {
-        "metric": METRIC, "value": round(gbs * world, 1), "unit": "GB/s", "n_gpus": world,
+        "metric": METRIC, "value": round(whole_job_rate(byts, ms, world) / 1e9, 1), "unit": "GB/s",
+        "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config,
@@ -425,7 +432,7 @@ def main():
     e2e_ms = max_over_ranks(e2e_ms, world)
     if rank != 0:
         return
-    tflops = flops / (ms * 1e-3) / 1e12 * world
+    tflops = whole_job_rate(flops, ms, world) / 1e12
     achieved = flops / (ms * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -438,7 +445,7 @@ def main():
                      "peak_source": peaks["source"] + " bf16 burst",
                      "kernel": "varlen_fwd_kernel<%d,%d>" % (w.d_qk, w.d_v),
                      "alg_flops_per_launch": flops, "alg_bytes_per_launch": byts},
-        "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(whole_job_rate(flops, e2e_ms, world) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": a.steps,
         "clocks": clocks,

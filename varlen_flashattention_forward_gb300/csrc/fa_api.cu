@@ -221,15 +221,16 @@ extern "C" fa_status fa_sparse_mla_decode(const void* q, const void* kv_cache,
   fa_status st = device_info(&dev);
   if (st != FA_OK) return st;
   if (num_tokens == 0) return FA_OK;
-  // Q viewed as [tokens, heads, 576]; a box covers one token, 64 heads
+  // Q viewed as [tokens, heads, 576]; a box covers one token, np heads
   // (heads past num_heads read as zero) and 64 columns.
+  const int np = num_heads >= 64 ? 64 : (num_heads <= 16 ? 16 : num_heads);
   CUtensorMap qmap;
   {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return FA_ERR_LAUNCH;
     cuuint64_t dims[3] = {576, (cuuint64_t)num_heads, (cuuint64_t)num_tokens};
     cuuint64_t strides[2] = {576 * 2, (cuuint64_t)num_heads * 576 * 2};
-    cuuint32_t box[3] = {64u, 64u, 1u};
+    cuuint32_t box[3] = {64u, (cuuint32_t)np, 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     if (fn(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box,
            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -250,7 +251,10 @@ extern "C" fa_status fa_sparse_mla_decode(const void* q, const void* kv_cache,
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
   a.status = dev->status;
-  cudaError_t e = fa::launch_sparse_decode(qmap, a, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = np == 64 ? fa::launch_decode_np<64>(qmap, a, st_)
+                : np == 32 ? fa::launch_decode_np<32>(qmap, a, st_)
+                           : fa::launch_decode_np<16>(qmap, a, st_);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
