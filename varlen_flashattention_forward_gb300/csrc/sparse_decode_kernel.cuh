@@ -8,19 +8,22 @@
 //   Sᵀ[key, head]  = R[key, 0:576] · Q[head, 0:576]ᵀ     M = 64 keys, N = heads
 //   Oᵀ[dv, head]  += R[key, 0:512]ᵀ · Pᵀ[key, head]       M = 128 (x4 tiles of dv)
 //
-//   producer warps 4-7  gather 64 rows per tile with 16-byte cp.async into a
-//                       2-stage ring (128-byte swizzle, the UMMA K-major layout
-//                       for Sᵀ and the MN-major layout for Oᵀ);
-//   MMA warp 8          TMA-loads Q once and issues Sᵀ as soon as a tile has
-//                       landed and its Sᵀ buffer is free;
-//   MMA warp 9          issues Oᵀ += Rᵀ·Pᵀ as soon as Pᵀ is ready and
-//                       releases the stage (two issuers, so waiting for the
+//   gather warps 4-7    copy each 64-key tile into a 2-stage ring with 16-byte
+//                       cp.async, one 64-column chunk at a time (128-byte
+//                       swizzle: the UMMA K-major layout for Sᵀ and the
+//                       MN-major layout for Oᵀ), each chunk on its own barrier;
+//   MMA warp 8          TMA-loads Q once and issues the Sᵀ MMAs of a chunk as
+//                       soon as it has landed;
+//   MMA warp 9          issues Oᵀ += Rᵀ·Pᵀ as soon as Pᵀ is ready, one
+//                       128-column m-tile at a time, and releases each m-tile's
+//                       chunks as it completes (two issuers, so waiting for the
 //                       next gathered tile never delays the current PV);
-//   softmax warps 0-3   one thread per key of the tile: per-head maximum over
-//                       the tile's keys (shuffle transpose-reduce + shared
-//                       memory), exp2 with a lazily rescaled running maximum,
-//                       per-thread partial row sums, and Pᵀ (bf16) written into
-//                       the tile's rope columns, which are dead once Sᵀ is done.
+//   softmax warps 0-3   two threads per key of the tile, each with half of the
+//                       heads: per-head maximum over the tile's keys (shuffle
+//                       transpose-reduce + shared memory), exp2 with a lazily
+//                       rescaled running maximum, per-thread partial row sums,
+//                       and Pᵀ (bf16) written into the tile's rope columns,
+//                       which are dead once Sᵀ is done.
 //
 // TMEM: Sᵀ double buffer at columns [0, 2*NP) (64-row layout: key r lives in
 // lane 32*(r/16) + r%16), Oᵀ at [128, 128 + 4*NP) (row = lane).
@@ -44,16 +47,17 @@ namespace fa {
 constexpr int kDecodePage = 64;
 constexpr int kDecodeThreads = 384;   // softmax 0-3, gather 4-7, S issuer 8, PV issuer 9, idle 10-11
 // Register split (launch: 168 x 384 = 64512): softmax 128 x 240, gather
-// 128 x 88, control 128 x 56 = 49152.
+// 128 x 88, control 128 x 96 = 54272.
 constexpr uint32_t kDecodeSoftmaxRegs = 240;
 constexpr uint32_t kDecodeGatherRegs = 88;
-constexpr uint32_t kDecodeControlRegs = 56;
+constexpr uint32_t kDecodeControlRegs = 96;
 constexpr int kDecodeKeys = 64;       // keys per tile
 constexpr int kDecodeMaxTopk = 2048;  // row table held in shared memory
 constexpr int kDqk = 576, kDv = 512;
-constexpr int kRowBytes = kDqk * 2;                       // 1152
+constexpr int kChunks = 9;            // 64-column chunks of a row: 8 latent + 1 rope
+constexpr int kPvGroups = 4;          // PV m-tiles of 128 value columns
 constexpr int kChunkBytes = kDecodeKeys * 128;            // one 64-column chunk
-constexpr int kStageBytes = 9 * kChunkBytes;              // 73728
+constexpr int kStageBytes = kChunks * kChunkBytes;        // 73728
 constexpr int kQBytes = 9 * 64 * 128;                     // Q for up to 64 heads
 
 struct DecodeArgs {
@@ -68,10 +72,15 @@ struct DecodeArgs {
   unsigned int* status;
 };
 
-struct alignas(8) DecodeCtl {
+// Chunk c of a stage is released when the PV m-tile that last reads it is
+// done: m-tile g reads value chunks 2g and 2g+1, and every m-tile reads Pᵀ
+// in the rope chunk 8, so chunk 8 goes with the last m-tile.
+__host__ __device__ constexpr int release_group(int c) { return c < 8 ? c >> 1 : kPvGroups - 1; }
+
+struct alignas(16) DecodeCtl {
   uint64_t q_full;
-  uint64_t r_full[2];
-  uint64_t r_free[2];
+  uint64_t r_full[2][kChunks];     // chunk landed (128 gather-thread arrivals)
+  uint64_t r_free[2][kPvGroups];   // the chunks of PV m-tile g may be overwritten
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full[2];   // Pᵀ(j) written, indexed by j % 2
@@ -79,15 +88,17 @@ struct alignas(8) DecodeCtl {
   uint64_t drain;
   uint32_t tmem_base;
   volatile int abort_flag;
-  float red[4][64];   // per-warp partial maxima / sums
+  alignas(16) float red[4][64];  // per-warp partial maxima / sums
   float m_used[64];   // running maximum per head (scaled log2 units)
-  float alpha[64];    // rescale factor of the current tile
-  float l_tot[64];    // final row sums
+  alignas(16) float alpha[64];   // rescale factors of the current tile; after the
+                                 // last tile, the reciprocal row sums
 };
 
 constexpr size_t kDecodeSmem = 1024 + kQBytes + 2 * kStageBytes +
                                sizeof(int) * kDecodeMaxTopk + sizeof(DecodeCtl);
 static_assert(kDecodeSmem <= 232448, "decode shared memory exceeds the per-CTA limit");
+static_assert((kQBytes + 2 * kStageBytes + sizeof(int) * kDecodeMaxTopk) % 16 == 0,
+              "control block must stay 16-byte aligned");
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -129,23 +140,40 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Max (kMax) or sum over the 16 lanes of each half-warp of NP values per
-// lane, by repeated halving: after the call lane l holds, in v[0 .. NP/16),
-// the reduction for heads [l*NP/16, (l+1)*NP/16).
-template <int NP, bool kMax>
+// Max (kMax) or sum of V values per lane over the 16 lanes of each half-warp
+// (the halves reduce independently), by repeated halving.  Afterwards a lane
+// holds max(V / 16, 1) results in v[0 ..); their value indices are given by
+// half_reduce_index.
+template <int V, bool kMax>
 __device__ __forceinline__ void half_warp_transpose_reduce(float* v, int lane) {
 #pragma unroll
-  for (int o = 8, n = NP; o >= 1; o >>= 1, n >>= 1) {
-    const int half = n / 2;
-    const bool upper = (lane & o) != 0;
+  for (int s = 0; s < 4; ++s) {
+    const int o = 8 >> s;
+    const int n = V >> s;  // values held before this step
+    if (n >= 2) {
+      const int half = n / 2;
+      const bool upper = (lane & o) != 0;
 #pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = upper ? v[i] : v[i + half];
-      const float keep = upper ? v[i + half] : v[i];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, o);
-      v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+      for (int i = 0; i < half; ++i) {
+        const float send = upper ? v[i] : v[i + half];
+        const float keep = upper ? v[i + half] : v[i];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+        v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+      }
+    } else {
+      const float recv = __shfl_xor_sync(0xffffffffu, v[0], o);
+      v[0] = kMax ? fmaxf(v[0], recv) : v[0] + recv;
     }
   }
+}
+template <int V>
+__device__ __forceinline__ int half_reduce_index(int lane, int i) {
+  return V >= 16 ? (lane & 15) * (V / 16) + i : ((lane & 15) >> 1);
+}
+// Lanes that publish the results (for V = 8, lane pairs hold the same one).
+template <int V>
+__device__ __forceinline__ bool half_reduce_writer(int lane) {
+  return V >= 16 || (lane & 1) == 0;
 }
 
 template <int NP>
@@ -155,7 +183,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   constexpr uint32_t kSwP = NP == 64 ? ptx::kLayoutSw128 : (NP == 32 ? ptx::kLayoutSw64
                                                                      : ptx::kLayoutSw32);
   constexpr int kPRowBytes = NP * 2;  // one Pᵀ row (one key) in bytes
-  constexpr int kPerLane = NP / 16;   // heads per lane after the transpose-reduce
+  constexpr int HP = NP / 2;          // heads per softmax thread
+  constexpr int kRed = HP >= 16 ? HP / 16 : 1;  // reduced values per lane
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -179,12 +208,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   if (tid == 0) {
     ptx::mbar_init(ptx::smem_u32(&cb->q_full), 1);
     for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&cb->r_full[s]), 128);
-      ptx::mbar_init(ptx::smem_u32(&cb->r_free[s]), 1);
+      for (int c = 0; c < kChunks; ++c) ptx::mbar_init(ptx::smem_u32(&cb->r_full[s][c]), 128);
+      for (int g = 0; g < kPvGroups; ++g) ptx::mbar_init(ptx::smem_u32(&cb->r_free[s][g]), 1);
       ptx::mbar_init(ptx::smem_u32(&cb->s_full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&cb->s_free[s]), 128);
-    }
-    for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(ptx::smem_u32(&cb->p_full[s]), 128);
       ptx::mbar_init(ptx::smem_u32(&cb->pv_done[s]), 1);
     }
@@ -198,18 +225,28 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   }
   // Row table: physical cache row of every top-k slot, -1 if the slot is
   // outside the token's context or its page is out of range.
+  // All index loads are issued before any page-table load, so the table
+  // costs two dependent memory round trips.
   {
+    constexpr int kPer = (kDecodeMaxTopk + kDecodeThreads - 1) / kDecodeThreads;
     const int64_t context = (int64_t)a.max_pages * kDecodePage;
     const int* idx = a.topk_idx + (size_t)token * a.topk;
     const int* pt = a.page_table + (size_t)token * a.max_pages;
-    for (int s = tid; s < a.topk; s += kDecodeThreads) {
-      const int p = idx[s];
-      int row = -1;
-      if (p >= 0 && p < context) {
-        const int page = pt[p / kDecodePage];
-        if (page >= 0 && page < a.num_pages) row = page * kDecodePage + p % kDecodePage;
-      }
-      rows[s] = row;
+    int p[kPer], page[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int s = tid + i * kDecodeThreads;
+      p[i] = s < a.topk ? __ldg(idx + s) : -1;
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      page[i] = (p[i] >= 0 && p[i] < context) ? __ldg(pt + p[i] / kDecodePage) : -1;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int s = tid + i * kDecodeThreads;
+      if (s < a.topk)
+        rows[s] = (page[i] >= 0 && page[i] < a.num_pages) ? page[i] * kDecodePage + p[i] % kDecodePage
+                                                          : -1;
     }
   }
   ptx::tc_fence_before();
@@ -220,32 +257,38 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   if (warp >= 4 && warp < 8) {
     ptx::regs_dec<kDecodeGatherRegs>();
     // ------------------------------------------------------------ gather
+    // Tile j goes to stage j % 2, one 64-column chunk at a time, so that the
+    // S MMAs can start on the first chunks while the rest are in flight.
+    // Each thread copies the same 16-byte unit (ptid % 8) of 4 rows
+    // (ptid / 8 + 16 i) per chunk; its copies of chunk c arrive on
+    // r_full[stage][c] by themselves when they land
+    // (cp.async.mbarrier.arrive.noinc; 128 arrivals expected), so no gather
+    // warp blocks on its own copies.  Chunk c of tile j >= 2 waits for the
+    // PV m-tile of tile j - 2 that last reads it.
     const int ptid = tid - 128;
-    // Tile j goes to stage j % 2.  Each gather thread's copies of tile j
-    // arrive on r_full[j % 2] by themselves when they land
-    // (cp.async.mbarrier.arrive.noinc; the barrier expects 128 arrivals), so
-    // no gather warp ever blocks on its own copies.  Stage reuse for tile j
-    // waits for PV(j - 2), which needs only tiles <= j - 1.
+    const int u = ptid & 7;
     bool ok = true;
     for (int j = 0; j < n_tiles && ok; ++j) {
-      if (j >= 2) {
-        ok = wait_warp(ptx::smem_u32(&cb->r_free[j & 1]), ((j >> 1) - 1) & 1, abort_flag,
-                       a.status);
-        if (!ok) break;
+      const int st = j & 1;
+      const uint32_t dst0 = ptx::smem_u32(stage[st]);
+      int row[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)  // invalid slots read row 0 (masked later)
+        row[i] = max(rows[j * kDecodeKeys + (ptid >> 3) + 16 * i], 0);
+      for (int c = 0; c < kChunks; ++c) {
+        if (j >= 2 && (c == 0 || (c < 8 && release_group(c) != release_group(c - 1)))) {
+          ok = wait_warp(ptx::smem_u32(&cb->r_free[st][release_group(c)]), ((j >> 1) - 1) & 1,
+                         abort_flag, a.status);
+          if (!ok) break;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = (ptid >> 3) + 16 * i;
+          ptx::cp_async_16(dst0 + c * kChunkBytes + r * 128 + ((u ^ (r & 7)) << 4),
+                           a.cache + (size_t)row[i] * kDqk + c * 64 + u * 8);
+        }
+        ptx::cp_async_mbar_arrive(ptx::smem_u32(&cb->r_full[st][c]));
       }
-      const uint32_t dst0 = ptx::smem_u32(stage[j & 1]);
-      const int* trow = rows + j * kDecodeKeys;
-#pragma unroll 4
-      for (int e = ptid; e < kDecodeKeys * 72; e += 128) {
-        const int r = e / 72;
-        const int c16 = e - r * 72;       // 16-byte unit within the row
-        const int row = max(trow[r], 0);  // invalid slots read row 0 (masked later)
-        const uint16_t* src = a.cache + (size_t)row * kDqk + c16 * 8;
-        const int chunk = c16 >> 3, u = c16 & 7;
-        const uint32_t dst = dst0 + chunk * kChunkBytes + r * 128 + ((u ^ (r & 7)) << 4);
-        ptx::cp_async_16(dst, src);
-      }
-      ptx::cp_async_mbar_arrive(ptx::smem_u32(&cb->r_full[j & 1]));
     }
     cp_async_wait<0>();  // nothing of this thread is in flight at exit
   } else if (warp >= 8) {
@@ -254,7 +297,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(64, NP, false, false);
     constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(128, NP, true, true);
     if (warp == 8 && lane == 0) {
-      // Sᵀ(j) = R(j) Qᵀ into Sᵀ buffer j % 2.
+      // Sᵀ(j) = R(j) Qᵀ into Sᵀ buffer j % 2, chunk by chunk as they land.
       ptx::prefetch_tmap(&q_map);
       ptx::mbar_arrive_expect_tx(ptx::smem_u32(&cb->q_full), 9 * NP * 128);
       for (int c = 0; c < 9; ++c)
@@ -263,53 +306,59 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       bool ok = wait_single(ptx::smem_u32(&cb->q_full), 0, abort_flag, a.status);
       const uint64_t qd = ptx::smem_desc(ptx::smem_u32(q_s), 16, 1024, ptx::kLayoutSw128);
       for (int j = 0; j < n_tiles && ok; ++j) {
-        ok = wait_single(ptx::smem_u32(&cb->r_full[j & 1]), (j >> 1) & 1, abort_flag, a.status);
-        if (ok && j >= 2)
-          ok = wait_single(ptx::smem_u32(&cb->s_free[j & 1]), ((j >> 1) - 1) & 1, abort_flag,
+        const int st = j & 1;
+        if (j >= 2) {
+          ok = wait_single(ptx::smem_u32(&cb->s_free[st]), ((j >> 1) - 1) & 1, abort_flag,
                            a.status);
-        if (!ok) break;
-        // The gathered rows were written by cp.async (generic proxy); order
-        // them before the tensor core's (async proxy) reads.
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_after();
-        const uint64_t rd =
-            ptx::smem_desc(ptx::smem_u32(stage[j & 1]), 16, 1024, ptx::kLayoutSw128);
-        const uint32_t d = tmem + (uint32_t)((j & 1) * NP);
-#pragma unroll
-        for (int k = 0; k < kDqk / 16; ++k) {
-          const uint32_t in = (k & 3) * 32;
-          ptx::mma_ss(d, ptx::desc_add(rd, (k >> 2) * kChunkBytes + in),
-                      ptx::desc_add(qd, (k >> 2) * NP * 128 + in), idesc_s, k > 0 ? 1u : 0u);
+          if (!ok) break;
         }
-        ptx::mma_commit(ptx::smem_u32(&cb->s_full[j & 1]));
+        const uint64_t rd = ptx::smem_desc(ptx::smem_u32(stage[st]), 16, 1024, ptx::kLayoutSw128);
+        const uint32_t d = tmem + (uint32_t)(st * NP);
+        for (int c = 0; c < kChunks && ok; ++c) {
+          ok = wait_single(ptx::smem_u32(&cb->r_full[st][c]), (j >> 1) & 1, abort_flag, a.status);
+          if (!ok) break;
+          // The gathered rows were written by cp.async (generic proxy); order
+          // them before the tensor core's (async proxy) reads.
+          ptx::fence_proxy_async_smem();
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            ptx::mma_ss(d, ptx::desc_add(rd, c * kChunkBytes + k * 32),
+                        ptx::desc_add(qd, c * NP * 128 + k * 32), idesc_s,
+                        (c > 0 || k > 0) ? 1u : 0u);
+        }
+        if (!ok) break;
+        ptx::mma_commit(ptx::smem_u32(&cb->s_full[st]));
       }
       ptx::mma_commit(ptx::smem_u32(&cb->drain));
       wait_single(ptx::smem_u32(&cb->drain), 0, abort_flag, a.status);
     } else if (warp == 9 && lane == 0) {
-      // Oᵀ += R(j)[:, 0:512]ᵀ Pᵀ(j), then release stage j % 2.
+      // Oᵀ += R(j)[:, 0:512]ᵀ Pᵀ(j), one 128-column m-tile at a time; each
+      // m-tile's commit releases the chunks it was the last to read.
       bool ok = true;
       for (int j = 0; j < n_tiles && ok; ++j) {
-        ok = wait_single(ptx::smem_u32(&cb->p_full[j & 1]), (j >> 1) & 1, abort_flag, a.status);
+        const int st = j & 1;
+        ok = wait_single(ptx::smem_u32(&cb->p_full[st]), (j >> 1) & 1, abort_flag, a.status);
         if (!ok) break;
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_after();
-        const uint32_t ra = ptx::smem_u32(stage[j & 1]);
+        const uint32_t ra = ptx::smem_u32(stage[st]);
         // A = R[keys, 128m .. 128m+128)ᵀ: MN-major, two 64-wide chunks.
         const uint64_t ad = ptx::smem_desc(ra, kChunkBytes, 1024, ptx::kLayoutSw128);
         // B = Pᵀ[keys, heads] in the rope chunk: MN-major, NP wide.
         const uint64_t bd =
             ptx::smem_desc(ra + 8 * kChunkBytes, 8 * kPRowBytes, 8 * kPRowBytes, kSwP);
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
+        for (int m = 0; m < kPvGroups; ++m) {
 #pragma unroll
           for (int k = 0; k < kDecodeKeys / 16; ++k)
             ptx::mma_ss(tmem + 128u + (uint32_t)(m * NP),
                         ptx::desc_add(ad, 2 * m * kChunkBytes + k * 16 * 128),
                         ptx::desc_add(bd, k * 16 * kPRowBytes), idesc_o,
                         (j > 0 || k > 0) ? 1u : 0u);
+          ptx::mma_commit(ptx::smem_u32(&cb->r_free[st][m]));
         }
-        ptx::mma_commit(ptx::smem_u32(&cb->pv_done[j & 1]));
-        ptx::mma_commit(ptx::smem_u32(&cb->r_free[j & 1]));
+        ptx::mma_commit(ptx::smem_u32(&cb->pv_done[st]));
       }
       ptx::mma_commit(ptx::smem_u32(&cb->drain));
       wait_single(ptx::smem_u32(&cb->drain), 0, abort_flag, a.status);
@@ -318,44 +367,50 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   } else {
     ptx::regs_inc<kDecodeSoftmaxRegs>();
     // ------------------------------------------------------------ softmax
-    const int key_in_tile = warp * 16 + (lane & 15);  // meaningful for lanes 0-15
-    const bool holds_key = lane < 16;
+    // Sᵀ has 64 key rows in TMEM lanes 32w + (0..15) of warp w's quarter.
+    // Lane l of warp w takes key 16w + l % 16 and heads [HP*(l/16), +HP).
+    const int half = lane >> 4;
+    const int key_in_tile = warp * 16 + (lane & 15);
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const float sl2 = a.scale_log2;
     const float neg_inf = -__int_as_float(0x7f800000);
-    float lpart[NP];
+    float lpart[HP];
 #pragma unroll
-    for (int h = 0; h < NP; ++h) lpart[h] = 0.f;
+    for (int h = 0; h < HP; ++h) lpart[h] = 0.f;
     if (tid < 64) cb->m_used[tid] = neg_inf;
     named_bar_sync(1, 128);
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
+      const int st = j & 1;
       // Every wait is followed by a warpgroup-wide agreement, so that no warp
       // can be left alone at a later named barrier after another gave up.
-      ok = wait_warp(ptx::smem_u32(&cb->s_full[j & 1]), (j >> 1) & 1, abort_flag, a.status);
+      ok = wait_warp(ptx::smem_u32(&cb->s_full[st]), (j >> 1) & 1, abort_flag, a.status);
       ok = named_bar_and(3, 128, ok);
       if (!ok) break;
       ptx::tc_fence_after();
-      uint32_t sr[NP];
-#pragma unroll
-      for (int c = 0; c < NP; c += 16) ptx::tmem_ld16(tmem + lane_base + (j & 1) * NP + c, sr + c);
+      uint32_t sr[HP];
+      ptx::tmem_ld_16x2<HP>(tmem + lane_base + st * NP, sr);
       ptx::tmem_wait_ld();
+      if constexpr (HP == 8) {
+        ptx::reg_fence8(sr);
+      } else {
 #pragma unroll
-      for (int c = 0; c < NP; c += 16) ptx::reg_fence16(sr + c);
+        for (int c = 0; c < HP; c += 16) ptx::reg_fence16(sr + c);
+      }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(ptx::smem_u32(&cb->s_free[j & 1]));  // Sᵀ buffer may be reused
-      const bool valid = holds_key && rows[j * kDecodeKeys + key_in_tile] >= 0;
-      float s[NP], v[NP];
+      ptx::mbar_arrive(ptx::smem_u32(&cb->s_free[st]));  // Sᵀ buffer may be reused
+      const bool valid = rows[j * kDecodeKeys + key_in_tile] >= 0;
+      float s[HP], v[HP];
 #pragma unroll
-      for (int h = 0; h < NP; ++h) {
+      for (int h = 0; h < HP; ++h) {
         s[h] = valid ? __uint_as_float(sr[h]) : neg_inf;
         v[h] = s[h];
       }
       // Per-head maximum over the tile: 16 lanes, then 4 warps.
-      half_warp_transpose_reduce<NP, true>(v, lane);
-      if (holds_key) {
+      half_warp_transpose_reduce<HP, true>(v, lane);
+      if (half_reduce_writer<HP>(lane)) {
 #pragma unroll
-        for (int i = 0; i < kPerLane; ++i) cb->red[warp][lane * kPerLane + i] = v[i];
+        for (int i = 0; i < kRed; ++i) cb->red[warp][half * HP + half_reduce_index<HP>(lane, i)] = v[i];
       }
       named_bar_sync(1, 128);
       int need = 0;
@@ -373,12 +428,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
       const int any = named_bar_or(2, 128, need);
       if (any) {
-        float al[NP];
 #pragma unroll
-        for (int h = 0; h < NP; ++h) {
-          al[h] = cb->alpha[h];
-          lpart[h] *= al[h];
-        }
+        for (int h = 0; h < HP; ++h) lpart[h] *= cb->alpha[half * HP + h];
         if (j > 0) {
           // Oᵀ holds the earlier tiles: wait for the last PV, then scale
           // every head column by its factor.
@@ -388,7 +439,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           if (!ok) break;
           ptx::tc_fence_after();
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
+          for (int m = 0; m < kPvGroups; ++m) {
 #pragma unroll
             for (int c = 0; c < NP; c += 16) {
               uint32_t o[16];
@@ -397,52 +448,56 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               ptx::tmem_wait_ld();
               ptx::reg_fence16(o);
 #pragma unroll
-              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al[c + i]);
+              for (int i = 0; i < 16; ++i)
+                o[i] = __float_as_uint(__uint_as_float(o[i]) * cb->alpha[c + i]);
               ptx::tmem_st16(addr, o);
             }
           }
           ptx::tmem_wait_st();
         }
       }
-      // Probabilities and Pᵀ row for this thread's key.
-      if (holds_key) {
-        uint8_t* prow = stage[j & 1] + 8 * kChunkBytes + key_in_tile * kPRowBytes;
+      // Probabilities: this thread's half of the Pᵀ row of its key.
+      {
+        uint8_t* prow = stage[st] + 8 * kChunkBytes + key_in_tile * kPRowBytes;
 #pragma unroll
-        for (int g = 0; g < NP / 8; ++g) {
+        for (int g = 0; g < HP / 8; ++g) {
           uint32_t pk[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const int h0 = g * 8 + 2 * i;
-            const float b0 = cb->m_used[h0], b1 = cb->m_used[h0 + 1];
+            const int h0 = g * 8 + 2 * i;  // local head index
+            const float b0 = cb->m_used[half * HP + h0], b1 = cb->m_used[half * HP + h0 + 1];
             const float p0 = valid ? ptx::ex2(fmaf(s[h0], sl2, -b0)) : 0.f;
             const float p1 = valid ? ptx::ex2(fmaf(s[h0 + 1], sl2, -b1)) : 0.f;
             lpart[h0] += p0;
             lpart[h0 + 1] += p1;
             pk[i] = ptx::pack_bf16x2(p0, p1);
           }
-          // Swizzled 16-byte unit g of row key_in_tile (pattern of the
-          // NP*2-byte-wide layout: unit index XOR row bits).
-          const int unit = kPerLane == 4 ? (g ^ (key_in_tile & 7))
-                                         : (kPerLane == 2 ? (g ^ ((key_in_tile >> 1) & 3))
-                                                          : (g ^ ((key_in_tile >> 2) & 1)));
+          // Swizzled 16-byte unit of row key_in_tile (the NP*2-byte-wide
+          // layout: unit index XOR row bits).
+          const int gu = half * (HP / 8) + g;
+          const int unit = NP == 64 ? (gu ^ (key_in_tile & 7))
+                                    : (NP == 32 ? (gu ^ ((key_in_tile >> 1) & 3))
+                                                : (gu ^ ((key_in_tile >> 2) & 1)));
           *reinterpret_cast<uint4*>(prow + unit * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(ptx::smem_u32(&cb->p_full[j & 1]));
+      ptx::mbar_arrive(ptx::smem_u32(&cb->p_full[st]));
     }
+    float* l_inv = cb->alpha;  // no longer needed as rescale factors
     if (ok) {
       // Row sums: reduce the per-thread partials over keys (16 lanes, 4 warps).
-      half_warp_transpose_reduce<NP, false>(lpart, lane);
-      if (holds_key) {
+      half_warp_transpose_reduce<HP, false>(lpart, lane);
+      if (half_reduce_writer<HP>(lane)) {
 #pragma unroll
-        for (int i = 0; i < kPerLane; ++i) cb->red[warp][lane * kPerLane + i] = lpart[i];
+        for (int i = 0; i < kRed; ++i)
+          cb->red[warp][half * HP + half_reduce_index<HP>(lane, i)] = lpart[i];
       }
       named_bar_sync(1, 128);
       if (tid < NP) {
         const float l = (cb->red[0][tid] + cb->red[1][tid]) + (cb->red[2][tid] + cb->red[3][tid]);
-        cb->l_tot[tid] = l;
+        l_inv[tid] = l > 0.f ? 1.f / l : 0.f;
         if (a.lse && tid < heads) {
           const float m = cb->m_used[tid];
           a.lse[(size_t)(head0 + tid) * a.num_tokens + token] =
@@ -454,29 +509,40 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       // means all of Oᵀ is final.
       ok = wait_warp(ptx::smem_u32(&cb->pv_done[(n_tiles - 1) & 1]), ((n_tiles - 1) >> 1) & 1,
                      abort_flag, a.status);
+      ok = named_bar_and(3, 128, ok);
     }
     if (ok) {
       ptx::tc_fence_after();
-      // Epilogue: lane = dv row within each 128-row tile of Oᵀ.
+      // Epilogue.  Oᵀ has one value column per TMEM lane, the output wants
+      // value columns contiguous per head.  Each thread packs heads (2k,
+      // 2k+1) of its column into one bf16x2 word and swaps words with the
+      // neighbouring lane, after which the even lane holds columns (c, c+1)
+      // of head 2k and the odd lane those of head 2k+1: one 4-byte store each.
+      float li[NP];
+#pragma unroll
+      for (int h = 0; h < NP; h += 4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(l_inv + h);
+        li[h] = v4.x; li[h + 1] = v4.y; li[h + 2] = v4.z; li[h + 3] = v4.w;
+      }
+      const bool odd = lane & 1;
+      uint16_t* out_g = a.out + ((size_t)token * a.num_heads + head0) * kDv;
 #pragma unroll 1
-      for (int m = 0; m < 4; ++m) {
-        const int dv = m * 128 + warp * 32 + lane;
+      for (int m = 0; m < kPvGroups; ++m) {
+        const int dv_even = m * 128 + warp * 32 + (lane & ~1);
+        uint32_t o[NP];
 #pragma unroll
-        for (int c = 0; c < NP; c += 16) {
-          uint32_t o[16];
-          ptx::tmem_ld16(tmem + lane_base + 128u + m * NP + c, o);
-          ptx::tmem_wait_ld();
-          ptx::reg_fence16(o);
+        for (int c = 0; c < NP; c += 16) ptx::tmem_ld16(tmem + lane_base + 128u + m * NP + c, o + c);
+        ptx::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int h = c + i;
-            if (h < heads) {
-              const float l = cb->l_tot[h];
-              const float val = l > 0.f ? __uint_as_float(o[i]) / l : 0.f;
-              const uint32_t b = ptx::pack_bf16x2(val, 0.f) & 0xffffu;
-              a.out[((size_t)token * a.num_heads + head0 + h) * kDv + dv] = (uint16_t)b;
-            }
-          }
+        for (int c = 0; c < NP; c += 16) ptx::reg_fence16(o + c);
+#pragma unroll
+        for (int k = 0; k < NP / 2; ++k) {
+          const uint32_t w = ptx::pack_bf16x2(__uint_as_float(o[2 * k]) * li[2 * k],
+                                              __uint_as_float(o[2 * k + 1]) * li[2 * k + 1]);
+          const uint32_t r = __shfl_xor_sync(0xffffffffu, w, 1);
+          const uint32_t pair = odd ? __byte_perm(w, r, 0x3276) : __byte_perm(w, r, 0x5410);
+          const int h = 2 * k + (odd ? 1 : 0);
+          if (h < heads) *reinterpret_cast<uint32_t*>(out_g + (size_t)h * kDv + dv_even) = pair;
         }
       }
     }
