@@ -127,8 +127,15 @@ fa_status fa_varlen_fwd(const void* q, const void* k, const void* v,
  *   out           bf16 [num_tokens, num_heads, 512]: sum_j p_j * row_j[0:512]
  *   lse           fp32 [num_heads, num_tokens] or NULL
  *
+ * The (token, head group, 64-key tile) work is spread evenly over the SMs;
+ * when a token's keys end up on several CTAs, their partial results go to a
+ * workspace allocated stream-ordered on `stream` (from a pool the library
+ * keeps for the device) and a second kernel merges them by their
+ * log-sum-exp [flash_attn] (FA4SplitKVCombineKernel).  Both launches and the workspace's
+ * allocation and release are ordered on `stream`.
+ *
  * Host errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (heads, topk),
- * FA_ERR_ARCH.
+ * FA_ERR_ARCH, FA_ERR_LAUNCH (launch or workspace allocation failed).
  */
 fa_status fa_sparse_mla_decode(const void* q, const void* kv_cache,
                                const int* page_table, const int* topk_idx,

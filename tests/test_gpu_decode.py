@@ -97,3 +97,33 @@ def test_full_size_sampled_rows(cuda_device):
         np.arange(d.num_heads), (d.num_tokens - 1) * d.num_heads + np.arange(d.num_heads)]))
     compare(q, cache, pt, ti, d.softmax_scale, rows=rows, out=out, lse=lse)
     assert fa.fa_get_device_status() == fa.FA_OK
+
+
+# Work-split schedules.  The host cuts the (token, head group) units' 64-key
+# tiles into per-CTA ranges either on unit boundaries (many units) or into
+# equal tile counts whose cut units are merged by their LSE (few units).
+@pytest.mark.parametrize("T,H,topk,context", [
+    (1, 64, 2048, 4096),    # one unit cut into 16 parts (2 tiles per CTA)
+    (1, 128, 512, 1024),    # two head groups, each cut into parts
+    (5, 32, 1024, 2048),    # parts of 2-3 CTAs, 32-head group
+    (7, 8, 384, 1024),      # 8 heads (16-wide group), odd tile counts
+])
+def test_split_schedules_elementwise(cuda_device, T, H, topk, context):
+    q, cache, pt, ti, scale = small_inputs(T, H, topk, context, seed=T * 1000 + H)
+    compare(q, cache, pt, ti, scale)
+
+
+def test_whole_unit_ranges_many_segments(cuda_device):
+    """300 tokens at top-k 128: about two whole units per CTA, so every CTA
+    reloads Q and hands its O accumulator over between segments."""
+    q, cache, pt, ti, scale = small_inputs(300, 64, 128, 512, seed=5)
+    rows = np.arange(300 * 64)
+    compare(q, cache, pt, ti, scale, rows=rows[::7])
+
+
+def test_split_with_invalid_part(cuda_device):
+    """One part of a cut unit has no valid key (LSE -inf): its weight is 0."""
+    q, cache, pt, ti, scale = small_inputs(1, 64, 2048, 4096, seed=21)
+    ti = ti.clone()
+    ti[0, 128:256] = -1   # tiles 2-3 (one CTA's whole range) invalid
+    compare(q, cache, pt, ti, scale)

@@ -2,8 +2,11 @@
 // argument validation, TMA descriptor encoding, dispatch over the compiled
 // head-dim instantiations, and the device status word.
 //
-// No function here allocates device memory, copies data or synchronises,
-// except fa_get_device_status (documented as synchronising).
+// No function here copies data or synchronises, except fa_get_device_status
+// (documented as synchronising).  The only device memory allocated is the
+// partial-result workspace of fa_sparse_mla_decode, stream-ordered from a
+// library-owned pool that keeps its memory between calls.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -38,6 +41,7 @@ struct DeviceInfo {
   bool arch_ok = false;
   int sm_count = 0;
   unsigned int* status = nullptr;  // device address of g_fa_status
+  cudaMemPool_t pool = nullptr;    // decode workspace pool, created on first need
 };
 
 std::mutex g_mu;
@@ -107,6 +111,31 @@ bool encode_rows(CUtensorMap* m, const void* base, int dim, int heads, int token
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The device's workspace pool: memory freed back to it stays reserved
+// (release threshold = max), so steady-state calls do not reach the driver's
+// allocator.
+cudaMemPool_t workspace_pool(DeviceInfo* d) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!d->pool) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof props);
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+    uint64_t keep = UINT64_MAX;
+    if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      return nullptr;
+    }
+    d->pool = pool;
+  }
+  return d->pool;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -197,12 +226,25 @@ extern "C" fa_status fa_varlen_fwd(const void* q, const void* k, const void* v,
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-extern "C" fa_status fa_sparse_mla_decode(const void* q, const void* kv_cache,
-                                          const int* page_table, const int* topk_idx,
-                                          int num_tokens, int num_heads, int topk,
-                                          int num_pages, int max_pages_per_tok,
-                                          float softmax_scale, void* out, float* lse,
-                                          fa_stream_t stream) {
+namespace {
+
+// Everything fa_sparse_mla_decode does before it needs workspace memory:
+// argument checks, the Q tensor map, the kernel arguments and the work split
+// (see the comment below).  `*launch` is false when there is nothing to run.
+struct DecodePlan {
+  fa::DecodeArgs a;
+  CUtensorMap qmap;
+  int np = 64;          // head group width the kernel is instantiated for
+  bool launch = false;
+  bool split = false;   // partial results and the merge kernel are needed
+  size_t o_bytes = 0;   // workspace: partial O, then partial LSE
+  size_t l_bytes = 0;
+};
+
+fa_status plan_decode(const void* q, const void* kv_cache, const int* page_table,
+                      const int* topk_idx, int num_tokens, int num_heads, int topk,
+                      int num_pages, int max_pages_per_tok, float softmax_scale, void* out,
+                      float* lse, DecodePlan* plan) {
   if (!q || !kv_cache || !page_table || !topk_idx || !out) return FA_ERR_INVALID_ARG;
   if (num_tokens < 0 || num_pages < 1 || max_pages_per_tok < 1 || topk < 1)
     return FA_ERR_INVALID_ARG;
@@ -217,14 +259,20 @@ extern "C" fa_status fa_sparse_mla_decode(const void* q, const void* kv_cache,
       (int64_t)topk > (int64_t)max_pages_per_tok * fa::kDecodePage)
     return FA_ERR_UNSUPPORTED;
   if ((int64_t)num_pages * fa::kDecodePage > INT32_MAX) return FA_ERR_UNSUPPORTED;
+  const int groups = (num_heads + 63) / 64;
+  const int n_tiles = topk / fa::kDecodeKeys;
+  const long long units = (long long)num_tokens * groups;
+  const long long total = units * n_tiles;
+  if (total > INT32_MAX) return FA_ERR_UNSUPPORTED;
   DeviceInfo* dev = nullptr;
   fa_status st = device_info(&dev);
   if (st != FA_OK) return st;
-  if (num_tokens == 0) return FA_OK;
+  plan->launch = num_tokens > 0;
+  if (!plan->launch) return FA_OK;
   // Q viewed as [tokens, heads, 576]; a box covers one token, np heads
   // (heads past num_heads read as zero) and 64 columns.
   const int np = num_heads >= 64 ? 64 : (num_heads <= 16 ? 16 : num_heads);
-  CUtensorMap qmap;
+  plan->np = np;
   {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return FA_ERR_LAUNCH;
@@ -232,12 +280,12 @@ extern "C" fa_status fa_sparse_mla_decode(const void* q, const void* kv_cache,
     cuuint64_t strides[2] = {576 * 2, (cuuint64_t)num_heads * 576 * 2};
     cuuint32_t box[3] = {64u, (cuuint32_t)np, 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
-    if (fn(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box,
-           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    if (fn(&plan->qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return FA_ERR_LAUNCH;
   }
-  fa::DecodeArgs a;
+  fa::DecodeArgs& a = plan->a;
   a.q = static_cast<const uint16_t*>(q);
   a.cache = static_cast<const uint16_t*>(kv_cache);
   a.page_table = page_table;
@@ -251,11 +299,82 @@ extern "C" fa_status fa_sparse_mla_decode(const void* q, const void* kv_cache,
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
   a.status = dev->status;
-  cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = np == 64 ? fa::launch_decode_np<64>(qmap, a, st_)
-                : np == 32 ? fa::launch_decode_np<32>(qmap, a, st_)
-                           : fa::launch_decode_np<16>(qmap, a, st_);
+  a.groups = groups;
+  a.n_tiles = n_tiles;
+  // Work split.  Each CTA takes a contiguous range of the (token, head group)
+  // units' 64-key tiles, at most kDecodeMaxTilesPerCta of them.  Either the
+  // ranges hold whole units, or they hold equal tile counts and the units cut
+  // by a range end are merged by a second kernel.  The host takes the cut
+  // with the fewer tiles on the busiest SM, counting the merge as
+  // kDecodeMergeCostTiles tiles.
+  const long long sms = dev->sm_count;
+  auto ceil_div = [](long long x, long long y) { return (x + y - 1) / y; };
+  // Whole units per CTA.
+  const long long upc = fa::kDecodeMaxTilesPerCta / n_tiles;
+  const long long grid_u = std::max(ceil_div(units, upc), std::min(units, sms));
+  const long long cost_u = ceil_div(grid_u, sms) * ceil_div(units, grid_u) * n_tiles;
+  // Equal tile counts, over whole waves of SMs, at least 2 tiles per CTA.
+  long long grid_t = ceil_div(total, fa::kDecodeMaxTilesPerCta * sms) * sms;
+  grid_t = std::min(grid_t, std::max(1LL, total / 2));
+  const bool cuts = units % grid_t != 0;
+  const long long cost_t = ceil_div(grid_t, sms) * ceil_div(total, grid_t) +
+                           (cuts ? fa::kDecodeMergeCostTiles : 0);
+  plan->split = cuts && cost_t < cost_u;
+  const long long grid = plan->split || !cuts ? grid_t : grid_u;
+  a.total_tiles = (int)total;
+  a.grid = (int)grid;
+  a.gran = plan->split || !cuts ? 1 : n_tiles;
+  const long long granules = total / a.gran;
+  a.range_q = (int)(granules / grid);
+  a.range_r = (int)(granules % grid);
+  a.part_o = nullptr;
+  a.part_lse = nullptr;
+  if (plan->split) {
+    plan->o_bytes = (size_t)2 * grid * 64 * fa::kDv * sizeof(float);
+    plan->l_bytes = (size_t)2 * grid * 64 * sizeof(float);
+  }
+  return FA_OK;
+}
+
+// Launches the planned kernels; `ws` holds plan.o_bytes + plan.l_bytes when
+// plan.split.
+fa_status launch_decode(DecodePlan& plan, void* ws, cudaStream_t stream) {
+  if (plan.split) {
+    plan.a.part_o = static_cast<float*>(ws);
+    plan.a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + plan.o_bytes);
+  }
+  const cudaError_t e = plan.np == 64 ? fa::launch_decode_np<64>(plan.qmap, plan.a, stream)
+                      : plan.np == 32 ? fa::launch_decode_np<32>(plan.qmap, plan.a, stream)
+                                      : fa::launch_decode_np<16>(plan.qmap, plan.a, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" fa_status fa_sparse_mla_decode(const void* q, const void* kv_cache,
+                                          const int* page_table, const int* topk_idx,
+                                          int num_tokens, int num_heads, int topk,
+                                          int num_pages, int max_pages_per_tok,
+                                          float softmax_scale, void* out, float* lse,
+                                          fa_stream_t stream) {
+  DecodePlan plan;
+  fa_status st = plan_decode(q, kv_cache, page_table, topk_idx, num_tokens, num_heads, topk,
+                             num_pages, max_pages_per_tok, softmax_scale, out, lse, &plan);
+  if (st != FA_OK || !plan.launch) return st;
+  cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  if (plan.split) {
+    DeviceInfo* dev = nullptr;
+    st = device_info(&dev);
+    if (st != FA_OK) return st;
+    cudaMemPool_t pool = workspace_pool(dev);
+    if (!pool) return FA_ERR_LAUNCH;
+    if (cudaMallocFromPoolAsync(&ws, plan.o_bytes + plan.l_bytes, pool, st_) != cudaSuccess)
+      return FA_ERR_LAUNCH;
+  }
+  st = launch_decode(plan, ws, st_);
+  if (ws && cudaFreeAsync(ws, st_) != cudaSuccess) st = FA_ERR_LAUNCH;
+  return st;
 }
 
 extern "C" fa_status fa_merge_attn_states(void* out, float* out_lse, const void* prefix_out,

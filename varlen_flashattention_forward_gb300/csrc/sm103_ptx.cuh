@@ -90,6 +90,37 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// Same, with an L2 cache policy (from make_policy_evict_first) attached.
+__device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst),
+               "l"(src), "l"(policy)
+               : "memory");
+}
+
+// L2 policy for data read once: its lines are the first to be evicted, so
+// they do not push out data that will be read again.
+__device__ __forceinline__ uint64_t make_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Drops a 128-byte global line from L2 without writing it back: for scratch
+// data that has been read for the last time.
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start before its predecessor ends; grid_dependency_wait
+// blocks until the predecessor grid has completed and its memory is visible.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // The mbarrier receives one arrival when all cp.async operations issued so
 // far by this thread have completed (the arrival is not pre-counted).
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
