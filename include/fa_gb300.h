@@ -63,7 +63,9 @@ typedef enum {
   FA_ERR_UNSUPPORTED = 2,   /* valid request outside what is compiled in */
   FA_ERR_ARCH = 3,          /* current device is not sm_103 (GB300) */
   FA_ERR_LAUNCH = 4,        /* CUDA launch or driver call failed */
-  FA_ERR_DEVICE_TIMEOUT = 5 /* reported by fa_get_device_status only */
+  FA_ERR_DEVICE_TIMEOUT = 5, /* reported by fa_get_device_status only */
+  FA_ERR_SCRATCH = 6        /* fa_sparse_mla_decode_noalloc: the call needs more
+                               scratch than its fixed buffer holds */
 } fa_status;
 
 /*
@@ -143,6 +145,38 @@ fa_status fa_sparse_mla_decode(const void* q, const void* kv_cache,
                                int num_pages, int max_pages_per_tok,
                                float softmax_scale, void* out, float* lse,
                                fa_stream_t stream);
+
+/*
+ * fa_sparse_mla_decode_noalloc -- fa_sparse_mla_decode without any device
+ * memory allocation.  The method's pages have no counterpart to this entry
+ * point: it serves callers that must not allocate (a fixed memory budget, or
+ * their own memory management).  Arguments, layouts, results and the other
+ * errors are those of fa_sparse_mla_decode; the same kernels run.
+ *
+ * When the work split cuts a token's keys between CTAs, the partial results
+ * go to one scratch buffer of fixed size (FA_NOALLOC_SCRATCH_BYTES) that the
+ * library holds in device memory (one per device) instead of a workspace
+ * allocation.  Nothing in it has to start at zero: every partial result is
+ * written before it is read, within the same call.
+ *
+ *   - A call whose split needs more scratch returns FA_ERR_SCRATCH and
+ *     launches nothing (fa_sparse_mla_decode handles it).
+ *   - Calls that can overlap in time on one device (different streams, or
+ *     different host threads) race on the shared scratch: the caller must
+ *     order them.
+ *   - The first call on each device does one-time setup (module load,
+ *     scratch address lookup, kernel attributes); make that first call
+ *     before any stream capture.
+ *
+ * Host errors: those of fa_sparse_mla_decode, and FA_ERR_SCRATCH.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (48u << 20)
+fa_status fa_sparse_mla_decode_noalloc(const void* q, const void* kv_cache,
+                                       const int* page_table, const int* topk_idx,
+                                       int num_tokens, int num_heads, int topk,
+                                       int num_pages, int max_pages_per_tok,
+                                       float softmax_scale, void* out, float* lse,
+                                       fa_stream_t stream);
 
 /*
  * fa_merge_attn_states -- merges two partial attention results of the same

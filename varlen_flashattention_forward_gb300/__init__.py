@@ -28,13 +28,15 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_ARCH = 3
 FA_ERR_LAUNCH = 4
 FA_ERR_DEVICE_TIMEOUT = 5
+FA_ERR_SCRATCH = 6
+NOALLOC_SCRATCH_BYTES = 48 << 20  # FA_NOALLOC_SCRATCH_BYTES
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
 
 # Exported C symbols (kept in sync with include/fa_gb300.h; a CPU test checks).
-EXPORTS = ("fa_varlen_fwd", "fa_sparse_mla_decode", "fa_merge_attn_states",
-           "fa_get_device_status", "fa_status_string")
+EXPORTS = ("fa_varlen_fwd", "fa_sparse_mla_decode", "fa_sparse_mla_decode_noalloc",
+           "fa_merge_attn_states", "fa_get_device_status", "fa_status_string")
 
 _lib = None
 
@@ -62,6 +64,9 @@ def load_library():
     lib.fa_sparse_mla_decode.argtypes = [p, p, p, p, i32, i32, i32, i32, i32,
                                          f32, p, p, p]
     lib.fa_sparse_mla_decode.restype = i32
+    lib.fa_sparse_mla_decode_noalloc.argtypes = [p, p, p, p, i32, i32, i32, i32, i32,
+                                                 f32, p, p, p]
+    lib.fa_sparse_mla_decode_noalloc.restype = i32
     lib.fa_merge_attn_states.argtypes = [p, p, p, p, p, p, i32, i32, i32, p]
     lib.fa_merge_attn_states.restype = i32
     lib.fa_get_device_status.argtypes = []
@@ -180,6 +185,35 @@ def fa_sparse_mla_decode(q, kv_cache, page_table, topk_idx, softmax_scale=None,
     if st != FA_OK:
         raise FaError(st, "fa_sparse_mla_decode")
     return (out, lse) if lse is not None else out
+
+
+def fa_sparse_mla_decode_noalloc(q, kv_cache, page_table, topk_idx, softmax_scale, out,
+                                 lse=None, stream=None):
+    """fa_sparse_mla_decode_noalloc (include/fa_gb300.h): the same decode with
+    no device allocation, by the library or here.  `out` [T, H, 512] bf16 and
+    (optionally) `lse` [H, T] fp32 are caller-provided.  Overlapping calls on
+    one device race on the library's fixed scratch; the caller orders them."""
+    import torch
+    lib = load_library()
+    _check(q, "q", torch.bfloat16, 3)
+    _check(kv_cache, "kv_cache", torch.bfloat16, 3)
+    _check(page_table, "page_table", torch.int32, 2)
+    _check(topk_idx, "topk_idx", torch.int32, 2)
+    _check(out, "out", torch.bfloat16, 3)
+    if lse is not None:
+        _check(lse, "lse", torch.float32, 2)
+    T, H, dq = q.shape
+    if dq != 576 or kv_cache.shape[1] != 64 or kv_cache.shape[2] != 576:
+        raise ValueError("q must be [T, H, 576] and kv_cache [pages, 64, 576]")
+    if page_table.shape[0] != T or topk_idx.shape[0] != T or tuple(out.shape) != (T, H, 512):
+        raise ValueError("page_table / topk_idx / out must have one row per token")
+    st = lib.fa_sparse_mla_decode_noalloc(
+        _ptr(q), _ptr(kv_cache), _ptr(page_table), _ptr(topk_idx), T, H,
+        topk_idx.shape[1], kv_cache.shape[0], page_table.shape[1],
+        float(softmax_scale), _ptr(out), _ptr(lse), _stream_ptr(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_sparse_mla_decode_noalloc")
+    return out
 
 
 def fa_merge_attn_states(prefix_out, prefix_lse, suffix_out, suffix_lse, out=None,

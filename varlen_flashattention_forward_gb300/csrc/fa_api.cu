@@ -11,11 +11,13 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/fa_gb300.h"
+#include "decode_plan.h"
 #include "merge_kernel.cuh"
 #include "sparse_decode_kernel.cuh"
 #include "varlen_fwd_kernel.cuh"
@@ -351,6 +353,29 @@ fa_status launch_decode(DecodePlan& plan, void* ws, cudaStream_t stream) {
 
 }  // namespace
 
+namespace fa {
+
+static_assert(sizeof(DecodePlan) <= kDecodePlanBytes && alignof(DecodePlan) <= 128,
+              "decode plan storage");
+
+fa_status decode_plan(const void* q, const void* kv_cache, const int* page_table,
+                      const int* topk_idx, int num_tokens, int num_heads, int topk,
+                      int num_pages, int max_pages_per_tok, float softmax_scale, void* out,
+                      float* lse, void* plan, size_t* workspace_bytes, bool* launch) {
+  DecodePlan* p = new (plan) DecodePlan();
+  const fa_status st = plan_decode(q, kv_cache, page_table, topk_idx, num_tokens, num_heads, topk,
+                                   num_pages, max_pages_per_tok, softmax_scale, out, lse, p);
+  *launch = st == FA_OK && p->launch;
+  *workspace_bytes = p->split ? p->o_bytes + p->l_bytes : 0;
+  return st;
+}
+
+fa_status decode_launch(void* plan, void* workspace, cudaStream_t stream) {
+  return launch_decode(*static_cast<DecodePlan*>(plan), workspace, stream);
+}
+
+}  // namespace fa
+
 extern "C" fa_status fa_sparse_mla_decode(const void* q, const void* kv_cache,
                                           const int* page_table, const int* topk_idx,
                                           int num_tokens, int num_heads, int topk,
@@ -425,6 +450,9 @@ extern "C" const char* fa_status_string(fa_status s) {
     case FA_ERR_ARCH: return "device is not sm_103 (GB300)";
     case FA_ERR_LAUNCH: return "CUDA launch or driver call failed";
     case FA_ERR_DEVICE_TIMEOUT: return "a kernel pipeline wait timed out";
+    case FA_ERR_SCRATCH:
+      return "the call needs more partial-result scratch than fa_sparse_mla_decode_noalloc's "
+             "fixed buffer holds";
   }
   return "unknown status";
 }
