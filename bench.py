@@ -224,9 +224,12 @@ def time_varlen(w, steps, warmup, device, world):
     return times_ms, clk.summary(), e2e_ms, h2d, d2h
 
 
-def time_decode(d, steps, warmup, device):
+def time_decode(d, steps, warmup, device, world):
     """Device time of fa_sparse_mla_decode on the decode workload (inputs drawn
-    on the device for speed; parity is covered by the tests)."""
+    on the device for speed; parity is covered by the tests), and the end to
+    end time with the step's inputs (Q, page table, top-k indices) copied in
+    from pinned host memory and the output (O, LSE) copied back.  The latent
+    cache is resident state, as in serving, and is not copied."""
     import varlen_flashattention_forward_gb300 as fa
     page_table, topk = d.make_indices()
     g = torch.Generator(device=device).manual_seed(d.seed)
@@ -236,20 +239,74 @@ def time_decode(d, steps, warmup, device):
     out = torch.empty((d.num_tokens, d.num_heads, 512), dtype=torch.bfloat16, device=device)
     lse = torch.empty((d.num_heads, d.num_tokens), dtype=torch.float32, device=device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
     for _ in range(warmup):
         fa.fa_sparse_mla_decode(q, cache, pt, ti, d.softmax_scale, out, lse)
     torch.cuda.synchronize(device)
-    ts = []
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize(device)
     for i in range(steps):
-        flush.fill_(float(i))
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record()
+        flush.fill_(float(i))                     # evict the last step's rows from L2
+        starts[i].record(stream)
         fa.fa_sparse_mla_decode(q, cache, pt, ti, d.softmax_scale, out, lse)
-        e.record()
-        torch.cuda.synchronize(device)
-        ts.append(s.elapsed_time(e))
+        ends[i].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    ts = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+    hq, hpt, hti = q.cpu().pin_memory(), pt.cpu().pin_memory(), ti.cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hpt, hti))
+    d2h = sum(t.numel() * t.element_size() for t in (hout, hlse))
+    e2e_steps = max(3, min(steps, 10))
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    e_start.record(stream)
+    for i in range(e2e_steps):
+        flush.fill_(float(i))
+        q.copy_(hq, non_blocking=True)
+        pt.copy_(hpt, non_blocking=True)
+        ti.copy_(hti, non_blocking=True)
+        fa.fa_sparse_mla_decode(q, cache, pt, ti, d.softmax_scale, out, lse)
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+    e_end.record(stream)
+    torch.cuda.synchronize(device)
+    # The flush of each end-to-end step is taken out again.
+    f_start = torch.cuda.Event(enable_timing=True)
+    f_end = torch.cuda.Event(enable_timing=True)
+    f_start.record(stream)
+    for i in range(e2e_steps):
+        flush.fill_(float(i))
+    f_end.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = (e_start.elapsed_time(e_end) - f_start.elapsed_time(f_end)) / e2e_steps
+    if fa.fa_get_device_status() != fa.FA_OK:
+        raise RuntimeError("device status word set during timing")
     del cache
-    return ts
+    return ts, e2e_ms, h2d, d2h
+
+
+def decode_launches_per_step(d, sm_count):
+    """Kernel launches of one fa_sparse_mla_decode call: 1, or 2 when the host
+    picks the equal-tile split (whose cut units are merged by a second
+    kernel).  Mirrors the schedule choice in csrc/fa_api.cu (plan_decode)."""
+    groups = (d.num_heads + 63) // 64
+    n_tiles = d.topk // 64
+    units = d.num_tokens * groups
+    total = units * n_tiles
+    cdiv = lambda x, y: -(-x // y)
+    upc = 32 // n_tiles
+    grid_u = max(cdiv(units, upc), min(units, sm_count))
+    cost_u = cdiv(grid_u, sm_count) * cdiv(units, grid_u) * n_tiles
+    grid_t = min(cdiv(total, 32 * sm_count) * sm_count, max(1, total // 2))
+    cuts = units % grid_t != 0
+    cost_t = cdiv(grid_t, sm_count) * cdiv(total, grid_t) + (6 if cuts else 0)
+    return 2 if (cuts and cost_t < cost_u and grid_t >= 2) else 1
 
 
 def extra_lines(steps, warmup, device, peaks):
@@ -343,10 +400,12 @@ def main_decode(a, world, rank, local, peaks):
     import varlen_flashattention_forward_gb300 as fa
     fa.load_library()
     with ClockSampler(local) as clk:
-        times = time_decode(d, a.steps, a.warmup, device)
+        times, e2e_ms, h2d, d2h = time_decode(d, a.steps, a.warmup, device, world)
     ms = max_over_ranks(statistics.mean(times), world)
+    e2e_ms = max_over_ranks(e2e_ms, world)
     if rank != 0:
         return
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
     gbs = byts / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(whole_job_rate(byts, ms, world) / 1e9, 1), "unit": "GB/s",
@@ -360,7 +419,9 @@ def main_decode(a, world, rank, local, peaks):
                      "kernel": "sparse_decode_kernel<64>", "alg_bytes_per_launch": byts,
                      "alg_flops_per_launch": metrics.decode_flops(d)},
         "tflops": round(metrics.decode_flops(d) / (ms * 1e-3) / 1e12, 1),
-        "gpu_launches": a.steps, "clocks": clk.summary(),
+        "e2e": {"value": round(whole_job_rate(byts, e2e_ms, world) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": a.steps * decode_launches_per_step(d, sms), "clocks": clk.summary(),
     }
     if not a.no_cpu_baseline:
         rate, n, dt, threads = decode_oracle_rate(d, a.cpu_budget)
