@@ -38,6 +38,32 @@ from varlen_flashattention_forward_gb300 import metrics, workloads  # noqa: E402
 METRIC = "varlen attention fwd TFLOPS and % of GB300 BF16 tensor peak (decode: % HBM BW)"
 L2_FLUSH_BYTES = 512 << 20
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
+# the dominant kernel, from the ncu captures summarised in profiles/.  A value
+# holds only for the kernel source it was measured on (sha256 prefix of the
+# listed files); after any change the bench reports null until re-captured.
+_CSRC = os.path.join(REPO, "varlen_flashattention_forward_gb300", "csrc")
+MEASURED_TRAFFIC = {
+    # profiles/varlen_fwd_vit_full_d80.md
+    "vit_full_d80": (158.49e6, "f59cb8b98c16dc92", ["varlen_fwd_kernel.cuh", "sm103_ptx.cuh"]),
+    # profiles/sparse_decode_128tok.md: 32-token capture scaled by tokens to 128
+    "sparse_mla_decode": (326.2e6, "0fa673a185c193a3",
+                          ["sparse_decode_kernel.cuh", "sm103_ptx.cuh", "fa_api.cu"]),
+}
+
+
+def measured_traffic(workload: str):
+    import hashlib
+    entry = MEASURED_TRAFFIC.get(workload)
+    if entry is None:
+        return None
+    value, digest, files = entry
+    m = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(_CSRC, f), "rb") as fh:
+            m.update(fh.read())
+    return value if m.hexdigest()[:16] == digest else None
+
 
 def load_peaks():
     path = os.path.join(REPO, "MEASURED_PEAKS.json")
@@ -414,7 +440,9 @@ def main_decode(a, world, rank, local, peaks):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config,
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                     "traffic": (measured_traffic("sparse_mla_decode")
+                                 if d.num_tokens == 128 else None),
                      "peak_source": peaks["source"] + " HBM copy",
                      "kernel": "sparse_decode_kernel<64>", "alg_bytes_per_launch": byts,
                      "alg_flops_per_launch": metrics.decode_flops(d)},
@@ -502,7 +530,8 @@ def main():
         "data": "synthetic", "config": config,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
+                     "frac": round(achieved / peaks["bf16_tflops"], 4),
+                     "traffic": measured_traffic(w.name),
                      "peak_source": peaks["source"] + " bf16 burst",
                      "kernel": "varlen_fwd_kernel<%d,%d>" % (w.d_qk, w.d_v),
                      "alg_flops_per_launch": flops, "alg_bytes_per_launch": byts},
