@@ -355,7 +355,7 @@ def extra_lines(steps, warmup, device, peaks):
                      "roofline_frac": round(t_roof * 1e3 / ms, 4)}
     try:
         d = workloads.DecodeWorkload()
-        t = time_decode(d, steps, warmup, device)
+        t, _, _, _ = time_decode(d, steps, warmup, device, 1)
         ms = statistics.mean(t)
         byts = metrics.decode_alg_bytes(d)
         res["decode"] = {"ms": round(ms, 4), "gbs": round(byts / ms / 1e6, 1),

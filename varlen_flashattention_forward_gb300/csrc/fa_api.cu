@@ -197,7 +197,7 @@ extern "C" fa_status fa_varlen_fwd(const void* q, const void* k, const void* v,
   const int qt = tail_width(d_qk);
   bool ok = encode_rows(&maps.q_full, q, d_qk, num_heads, total_q, 64, fa::kBM) &&
             encode_rows(&maps.k_full, kb, d_qk, kh, tk, 64, fa::kBN) &&
-            encode_rows(&maps.v_full, vb, vd, kh, tk, 64, fa::kBN);
+            encode_rows(&maps.v_full, vb, vd, kh, tk, fa::v_atom_width(vd), fa::kBN);
   if (ok && qt)
     ok = encode_rows(&maps.q_tail, q, d_qk, num_heads, total_q, qt, fa::kBM) &&
          encode_rows(&maps.k_tail, kb, d_qk, kh, tk, qt, fa::kBN);

@@ -83,17 +83,28 @@ __host__ __device__ constexpr uint32_t layout_for_width(int w) {
   return w == 64 ? ptx::kLayoutSw128 : (w == 32 ? ptx::kLayoutSw64 : ptx::kLayoutSw32);
 }
 
+// Width (elements) of the swizzle atoms V is stored in: the widest of 64, 32
+// and 16 that divides d_v rounded up to 16, so that a V tile holds no padding
+// columns beyond that rounding (d_v = 80 is five 16-wide atoms, 20 KB per
+// 128 keys, instead of two zero-filled 64-wide atoms, 32 KB).  The host
+// encodes the V tensor map with the same box width.
+__host__ __device__ constexpr int v_atom_width(int d_v) {
+  return ((d_v + 15) / 16 * 16) % 64 == 0 ? 64 : (((d_v + 15) / 16 * 16) % 32 == 0 ? 32 : 16);
+}
+
 template <int D_QK, int D_V>
 struct VarlenCfg {
   using QK = HeadDim<D_QK>;
   using VD = HeadDim<D_V>;
   static constexpr int q_tile_bytes = QK::tile_bytes(kBM);
   static constexpr int k_tile_bytes = QK::tile_bytes(kBN);
-  // V is stored as whole 64-wide swizzle atoms (TMA zero-fills columns past
-  // d_v), so that P V is one N = d_v MMA per 16 keys: a tensor-core
-  // instruction costs about the same for any N up to 128.
-  static constexpr int v_chunks = (VD::padded + 63) / 64;
-  static constexpr int v_tile_bytes = v_chunks * kBN * 128;
+  // V is stored MN-major as v_atoms atoms of v_atom_width columns (TMA
+  // zero-fills columns past d_v), so that P V is one N = d_v MMA per 16 keys:
+  // a tensor-core instruction costs about the same for any N up to 128.
+  static constexpr int v_atom = v_atom_width(D_V);
+  static constexpr int v_atoms = VD::padded / v_atom;
+  static constexpr int v_atom_bytes = kBN * v_atom * 2;
+  static constexpr int v_tile_bytes = v_atoms * v_atom_bytes;
   static constexpr int slot_bytes =
       ((k_tile_bytes > v_tile_bytes ? k_tile_bytes : v_tile_bytes) + 1023) / 1024 * 1024;
   static constexpr int sched_bytes_max = 8 * (kMaxBatch + 1) + 4 * kVarlenThreads;
@@ -410,9 +421,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
               } else {
                 ptx::mbar_arrive_expect_tx(bar, C::v_tile_bytes);
 #pragma unroll
-                for (int c = 0; c < C::v_chunks; ++c)
-                  ptx::tma_load_3d(ptx::smem_u32(dst + c * kBN * 128), &maps.v_full, bar, c * 64,
-                                   w.kv_head, krow);
+                for (int c = 0; c < C::v_atoms; ++c)
+                  ptx::tma_load_3d(ptx::smem_u32(dst + c * C::v_atom_bytes), &maps.v_full, bar,
+                                   c * C::v_atom, w.kv_head, krow);
               }
               ++slot_issued[slot];
               if (++slot == NS) { slot = 0; phase ^= 1; }
@@ -491,15 +502,16 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         };
         auto issue_pv = [&](const uint8_t* vbuf, bool first) {
           // One MMA per 16 keys over all of d_v: MN-major B spanning
-          // C::v_chunks 64-wide atoms, kBN * 128 bytes apart.
+          // C::v_atoms atoms (LBO = atom stride), 8-key groups SBO apart.
           constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(kBM, VD::padded, false, true);
-          const uint64_t vd =
-              ptx::smem_desc(ptx::smem_u32(vbuf), kBN * 128, 1024, ptx::kLayoutSw128);
+          constexpr uint32_t kRowBytes = C::v_atom * 2;
+          const uint64_t vd = ptx::smem_desc(ptx::smem_u32(vbuf), C::v_atom_bytes, 8 * kRowBytes,
+                                             layout_for_width(C::v_atom));
           const uint32_t a0 = tmem + C::s_col(t);
 #pragma unroll
           for (int s = 0; s < kBN / 16; ++s)
-            ptx::mma_ts(tmem + C::o_col(t), a0 + s * 8, ptx::desc_add(vd, s * 16 * 128), idesc_pv,
-                        (!first || s > 0) ? 1u : 0u);
+            ptx::mma_ts(tmem + C::o_col(t), a0 + s * 8, ptx::desc_add(vd, s * 16 * kRowBytes),
+                        idesc_pv, (!first || s > 0) ? 1u : 0u);
         };
         // Both issuers walk every KV tile of every item (to stay in phase on
         // the ring); an issuer whose tile is absent from the item only waits
@@ -522,10 +534,10 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           if (mine) {
             issue_s(ring + slot * C::slot_bytes);
             ptx::mma_commit(ptx::smem_u32(&cb->s_full[t]));
-            if (w.n_kv == 1) ptx::mma_commit(ptx::smem_u32(&cb->q_free[t]));
           }
-          ptx::mma_commit(ptx::smem_u32(&cb->kv_free[slot]));
           pass_turn();
+          if (mine && w.n_kv == 1) ptx::mma_commit(ptx::smem_u32(&cb->q_free[t]));
+          ptx::mma_commit(ptx::smem_u32(&cb->kv_free[slot]));
           if (++slot == NS) { slot = 0; phase ^= 1; }
           for (int j = 0; j < w.n_kv && ok; ++j) {
             const int vslot = slot;
@@ -548,8 +560,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
               ptx::tc_fence_after();
               issue_pv(ring + vslot * C::slot_bytes, j == 0);
             }
+            int kslot = -1;
             if (has_next) {
-              const int kslot = slot;
+              kslot = slot;
               ok = wait_single(ptx::smem_u32(&cb->kv_full[kslot]), phase, abort_flag,
                                args.status);
               if (!ok) break;
@@ -558,14 +571,20 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                 ptx::tc_fence_after();
                 issue_s(ring + kslot * C::slot_bytes);
                 ptx::mma_commit(ptx::smem_u32(&cb->s_full[t]));
-                if (j + 2 == w.n_kv) ptx::mma_commit(ptx::smem_u32(&cb->q_free[t]));
               }
-              ptx::mma_commit(ptx::smem_u32(&cb->kv_free[kslot]));
             } else if (mine) {
               ptx::mma_commit(ptx::smem_u32(&cb->o_full[t]));
             }
-            ptx::mma_commit(ptx::smem_u32(&cb->kv_free[vslot]));
+            // The other issuer goes next; the commits that only release
+            // buffers follow (a commit tracks this thread's MMAs alone, and
+            // with the tensor-core queue full each costs issue time that
+            // would otherwise delay the other query tile's MMAs).
             pass_turn();
+            if (has_next) {
+              if (mine && j + 2 == w.n_kv) ptx::mma_commit(ptx::smem_u32(&cb->q_free[t]));
+              ptx::mma_commit(ptx::smem_u32(&cb->kv_free[kslot]));
+            }
+            ptx::mma_commit(ptx::smem_u32(&cb->kv_free[vslot]));
           }
         }
         // Drain: every MMA issued by either issuer completes before TMEM is
