@@ -627,34 +627,39 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         ++sn;
         if (!ok) break;
         ptx::tc_fence_after();
-        uint32_t sr[kBN];
+        // S through the sm_103 reducing TMEM load: the values and, per 32
+        // columns, their maximum.
+        float s[kBN], qmax[kBN / 32];
 #pragma unroll
-        for (int q = 0; q < kBN / 32; ++q) ptx::tmem_ld32(s_addr + q * 32, sr + q * 32);
+        for (int q = 0; q < kBN / 32; ++q) ptx::tmem_ld32_max(s_addr + q * 32, s + q * 32, qmax[q]);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < kBN / 16; ++q) ptx::reg_fence16(sr + q * 16);
-        float s[kBN];
+        for (int q = 0; q < kBN / 16; ++q) ptx::reg_fence16f(s + q * 16);
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) s[c] = __uint_as_float(sr[c]);
+        for (int q = 0; q < kBN / 32; ++q) ptx::reg_fence1f(qmax[q]);
 
         const int k0 = (w.tile_lo + j) * kBN;
-        if (!(k0 >= lo_i && k0 + kBN <= hi_i)) {
-          // Boundary tile for this row: mask keys outside [lo_i, hi_i).
+        float row_max;
+        if (k0 >= lo_i && k0 + kBN <= hi_i) {
+          // Every key of the tile is visible to this row: the hardware max.
+          row_max = ptx::max3(qmax[0], qmax[1], fmaxf(qmax[2], qmax[3]));
+        } else {
+          // Boundary tile for this row: mask keys outside [lo_i, hi_i) and
+          // reduce in software (the hardware max is over the unmasked S).
           const unsigned span = (unsigned)(hi_i - lo_i);
 #pragma unroll
           for (int c = 0; c < kBN; ++c)
             s[c] = ((unsigned)(k0 + c - lo_i) < span) ? s[c] : neg_inf;
+          float mx[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mx[k] = fmaxf(s[k], s[k + 4]);
+#pragma unroll
+          for (int c = 8; c < kBN; c += 8) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mx[k] = ptx::max3(mx[k], s[c + k], s[c + k + 4]);
+          }
+          row_max = ptx::max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
         }
-        // Row max: software reduction with 3-input max, 4 independent chains.
-        float mx[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) mx[k] = fmaxf(s[k], s[k + 4]);
-#pragma unroll
-        for (int c = 8; c < kBN; c += 8) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) mx[k] = ptx::max3(mx[k], s[c + k], s[c + k + 4]);
-        }
-        const float row_max = ptx::max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
         const float m_tile = row_max * sl2;  // -inf stays -inf
         const bool need = m_tile > m_used + kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
