@@ -10,11 +10,12 @@
 //                     O_t += P_t V_j          (TS form, P read from TMEM)
 //                   Two issuers keep the two tiles' chains independent: a
 //                   thread blocked on a full tensor-core queue while issuing
-//                   one tile's MMAs cannot delay the other tile.  They take
-//                   turns per issue group (tile 0 group g, tile 1 group g,
-//                   tile 0 group g+1, ...) so the tensor core alternates
-//                   between the tiles and each tile's softmax runs while the
-//                   other tile's MMAs execute (ping-pong).
+//                   one tile's MMAs cannot delay the other tile.  For
+//                   d_qk == d_v they take turns per issue group (tile 0 group
+//                   g, tile 1 group g, tile 0 group g+1, ...) so the tensor
+//                   core alternates between the tiles and each tile's softmax
+//                   runs while the other tile's MMAs execute (ping-pong);
+//                   for MLA shapes they run free (VarlenCfg::turns).
 //   softmax WG t    one thread per query row (TMEM lane): loads S_t with the
 //                   sm_103 reducing TMEM load (values + per-32-column max),
 //                   masks only boundary tiles (software 3-input max there),
@@ -143,6 +144,13 @@ struct VarlenCfg {
   static constexpr int nstage = nstage_fit > 8 ? 8 : nstage_fit;
   static_assert(nstage >= 2, "shared memory too small for two ring slots");
   static_assert(pv_n <= 128, "O accumulator wider than its TMEM region");
+  // Issue order between the two query tiles' MMA groups.  Strict turns
+  // (ping-pong) for d_qk == d_v, where a group is short and free-running
+  // issuers fall into lockstep (measured: ViT d80 0.57 vs 0.67 ms); free
+  // running for d_qk > d_v (MLA 192/128: long S groups, a two-slot ring),
+  // where turns cost more than they save (causal 4 x 4096: 794 vs 699
+  // TFLOP/s).
+  static constexpr bool turns = D_QK == D_V;
   // TMEM columns of the S/P and O regions of query tile t.
   __host__ __device__ static constexpr uint32_t s_col(int t) { return 128u * (uint32_t)t; }
   __host__ __device__ static constexpr uint32_t o_col(int t) { return 256u + 128u * (uint32_t)t; }
@@ -496,12 +504,12 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         uint32_t groups = 0;  // issue groups done by this issuer
         // Wait for this issuer's turn; issuer 0 starts.
         auto take_turn = [&]() -> bool {
-          if (t == 0 && groups == 0) return true;
+          if (!C::turns || (t == 0 && groups == 0)) return true;
           const uint32_t par = (t == 0 ? groups - 1 : groups) & 1;
           return wait_single(ptx::smem_u32(&cb->turn[t]), par, abort_flag, args.status);
         };
         auto pass_turn = [&]() {
-          ptx::mbar_arrive(ptx::smem_u32(&cb->turn[t ^ 1]));
+          if (C::turns) ptx::mbar_arrive(ptx::smem_u32(&cb->turn[t ^ 1]));
           ++groups;
         };
         int slot = 0;
