@@ -59,15 +59,16 @@ constexpr int kVarlenThreads = 384;   // 2 softmax warpgroups + {producer, 2 MMA
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;           // issuer of tile 0 (and TMEM owner); warp 10 issues tile 1
 // Register split (launch: 168 per thread x 384 threads = 64512):
-// softmax warpgroups 2 x 128 x 208 + control warpgroup 128 x 56 = 60416.
+// softmax warpgroups 2 x 128 x 208 + control warpgroup 128 x 64 = 61440.
 constexpr uint32_t kSoftmaxRegs = 208;
-constexpr uint32_t kControlRegs = 56;
+constexpr uint32_t kControlRegs = 64;
 constexpr int kBM = 128;              // query rows per tile
 constexpr int kBN = 128;              // keys per KV tile
 constexpr int kRowsPerItem = 2 * kBM; // two query tiles per work item
 constexpr int kMaxBatch = 1024;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold, log2 units
 constexpr int kSmemBudget = 232448;   // 227 KB opt-in per CTA
+constexpr int kBarrierBytes = 320;    // VarlenBarriers, reserved in the smem budget
 
 constexpr unsigned int kStatusTimeout = 1u;
 
@@ -139,8 +140,17 @@ struct VarlenCfg {
   static constexpr int slot_bytes =
       ((k_tile_bytes > v_region_bytes ? k_tile_bytes : v_region_bytes) + 1023) / 1024 * 1024;
   static constexpr int sched_bytes_max = 8 * (kMaxBatch + 1) + 4 * kVarlenThreads;
-  static constexpr int fixed_bytes = 1024 /*align*/ + 2 * q_tile_bytes + 256 /*barriers*/;
-  static constexpr int nstage_fit = (kSmemBudget - fixed_bytes - sched_bytes_max) / slot_bytes;
+  // Ring slots that fit next to `pairs` pairs of Q tiles.
+  static constexpr int ring_fit(int pairs) {
+    return (kSmemBudget - (1024 /*align*/ + pairs * 2 * q_tile_bytes + kBarrierBytes) -
+            sched_bytes_max) / slot_bytes;
+  }
+  // Two pairs of Q buffers, used by alternate work items, so that the next
+  // item's Q loads while the current item runs (a short sequence's item is
+  // only a few KV steps long, and its Q would otherwise wait for the
+  // current item's last S); only where six ring slots still fit.
+  static constexpr int q_pairs = ring_fit(2) >= 6 ? 2 : 1;
+  static constexpr int nstage_fit = ring_fit(q_pairs);
   static constexpr int nstage = nstage_fit > 8 ? 8 : nstage_fit;
   static_assert(nstage >= 2, "shared memory too small for two ring slots");
   static_assert(pv_n <= 128, "O accumulator wider than its TMEM region");
@@ -177,8 +187,8 @@ struct VarlenMaps {
 
 // Shared-memory control block (after the tiles).
 struct alignas(8) VarlenBarriers {
-  uint64_t q_full[2];
-  uint64_t q_free[2];
+  uint64_t q_full[4];  // [pair * 2 + tile]
+  uint64_t q_free[4];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_full[2];
@@ -190,6 +200,7 @@ struct alignas(8) VarlenBarriers {
   uint32_t tmem_base;
   volatile int abort_flag;
 };
+static_assert(sizeof(VarlenBarriers) <= kBarrierBytes, "barrier block larger than reserved");
 
 struct WorkItem {
   int q_start, k_start, lq, lk, head, kv_head, row0, n_qt, tile_lo, n_kv;
@@ -360,8 +371,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* q_tile[2] = {smem, smem + C::q_tile_bytes};
-  uint8_t* ring = smem + 2 * C::q_tile_bytes;
+  // Q tile t of buffer pair p at smem + (2p + t) * q_tile_bytes.
+  uint8_t* const q_base = smem;
+  uint8_t* ring = smem + 2 * C::q_pairs * C::q_tile_bytes;
   VarlenBarriers* cb = reinterpret_cast<VarlenBarriers*>(ring + NS * C::slot_bytes);
   int* s_prefix = reinterpret_cast<int*>(cb + 1);
   int* s_sorted = s_prefix + (args.batch + 1);
@@ -373,15 +385,16 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
   const int lane = tid & 31;
 
   if (tid == 0) {
+    for (int q = 0; q < 4; ++q) {
+      ptx::mbar_init(ptx::smem_u32(&cb->q_full[q]), 1);
+      ptx::mbar_init(ptx::smem_u32(&cb->q_free[q]), 1);
+    }
     for (int t = 0; t < 2; ++t) {
-      ptx::mbar_init(ptx::smem_u32(&cb->q_full[t]), 1);
       ptx::mbar_init(ptx::smem_u32(&cb->s_full[t]), 1);
       ptx::mbar_init(ptx::smem_u32(&cb->p_full[t]), kBM);
       ptx::mbar_init(ptx::smem_u32(&cb->o_full[t]), 1);
       ptx::mbar_init(ptx::smem_u32(&cb->o_free[t]), kBM);
     }
-    ptx::mbar_init(ptx::smem_u32(&cb->q_free[0]), 1);
-    ptx::mbar_init(ptx::smem_u32(&cb->q_free[1]), 1);
     ptx::mbar_init(ptx::smem_u32(&cb->drain), 2);
     ptx::mbar_init(ptx::smem_u32(&cb->turn[0]), 1);
     ptx::mbar_init(ptx::smem_u32(&cb->turn[1]), 1);
@@ -431,27 +444,34 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     if (warp == kProducerWarp) {
       // ---------------------------------------------------------- producer
       if (lane == 0) {
-        uint32_t qf_n[2] = {0, 0};
+        // Per Q buffer b = 2 * pair + tile, bit b: parity of the q_free
+        // phases consumed, of the Q loads issued, and whether any was issued.
+        uint32_t qf_par = 0, qi_par = 0, qi_any = 0;
+        uint32_t item_n = 0;  // items with KV tiles so far (selects the pair)
         int slot = 0;
         uint32_t phase = 0;
-        uint32_t q_issued[2] = {0, 0};
         uint32_t slot_issued[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         bool ok = true;
         for (int it = blockIdx.x; it < total_items && ok; it += gridDim.x) {
           const WorkItem w = decode_item(it, args, s_prefix, s_sorted);
           if (w.n_kv == 0) continue;
+          const int pair = C::q_pairs == 2 ? (int)(item_n & 1) : 0;
+          ++item_n;
           for (int t = 0; t < w.n_qt && ok; ++t) {
-            ok = wait_single(ptx::smem_u32(&cb->q_free[t]), (qf_n[t] & 1) ^ 1, abort_flag,
+            const int b = 2 * pair + t;
+            ok = wait_single(ptx::smem_u32(&cb->q_free[b]), ((qf_par >> b) & 1) ^ 1, abort_flag,
                              args.status);
-            ++qf_n[t];
+            qf_par ^= 1u << b;
             if (!ok) break;
-            const uint32_t bar = ptx::smem_u32(&cb->q_full[t]);
+            const uint32_t bar = ptx::smem_u32(&cb->q_full[b]);
             ptx::mbar_arrive_expect_tx(bar, C::q_tile_bytes);
-            ++q_issued[t];
+            qi_par ^= 1u << b;
+            qi_any |= 1u << b;
             const int row = w.q_start + w.row0 + t * kBM;
+            uint8_t* qdst = q_base + b * C::q_tile_bytes;
 #pragma unroll
             for (int c = 0; c < QK::chunks; ++c)
-              ptx::tma_load_3d(ptx::smem_u32(q_tile[t] + QK::chunk_off(c, kBM)),
+              ptx::tma_load_3d(ptx::smem_u32(qdst + QK::chunk_off(c, kBM)),
                                c < QK::full ? &maps.q_full : &maps.q_tail, bar, c * 64, w.head,
                                row);
           }
@@ -484,9 +504,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         }
         if (!ok) {
           // Let every copy this thread started land before the CTA exits.
-          for (int t = 0; t < 2; ++t)
-            if (q_issued[t])
-              wait_single(ptx::smem_u32(&cb->q_full[t]), (q_issued[t] - 1) & 1, abort_flag,
+          for (int b = 0; b < 4; ++b)
+            if ((qi_any >> b) & 1)
+              wait_single(ptx::smem_u32(&cb->q_full[b]), ((qi_par >> b) & 1) ^ 1, abort_flag,
                           args.status);
           for (int s = 0; s < NS; ++s)
             if (slot_issued[s])
@@ -500,7 +520,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
       if (lane == 0) {
         const int t = warp - kMmaWarp;  // query tile this thread issues for
         constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(kBM, kBN, false, false);
-        uint32_t qn = 0, pn = 0, ofn = 0;
+        uint32_t q_par = 0;   // bit b: parity of the q_full[b] phases consumed
+        uint32_t item_n = 0;  // items with KV tiles so far (selects the Q pair)
+        uint32_t pn = 0, ofn = 0;
         uint32_t groups = 0;  // issue groups done by this issuer
         // Wait for this issuer's turn; issuer 0 starts.
         auto take_turn = [&]() -> bool {
@@ -523,14 +545,14 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         // instruction count matters).
         constexpr uint32_t kQkTailSbo = 8 * (QK::tail ? QK::tail : 16) * 2;
         constexpr uint32_t kQkTailLay = layout_for_width(QK::tail ? QK::tail : 16);
-        uint64_t q_desc[2], q_desc_tail[2];
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const uint32_t qa = ptx::smem_u32(q_tile[t]);
-          q_desc[t] = ptx::smem_desc(qa, 16, 1024, ptx::kLayoutSw128);
-          q_desc_tail[t] =
+        // Descriptors of this issuer's Q tile in the current item's pair.
+        uint64_t q_desc = 0, q_desc_tail = 0;
+        auto set_q = [&](int b) {
+          const uint32_t qa = ptx::smem_u32(q_base + b * C::q_tile_bytes);
+          q_desc = ptx::smem_desc(qa, 16, 1024, ptx::kLayoutSw128);
+          q_desc_tail =
               ptx::smem_desc(qa + QK::chunk_off(QK::full, kBM), 16, kQkTailSbo, kQkTailLay);
-        }
+        };
         auto issue_s = [&](const uint8_t* kbuf) {
           const uint32_t d = tmem + C::s_col(t);
           const uint32_t ka = ptx::smem_u32(kbuf);
@@ -543,11 +565,11 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             if (c < QK::full) {
               // kBM == kBN: the same offset addresses Q and K chunks.
               const uint32_t off = (uint32_t)(QK::chunk_off(c, kBN) + ((s * 16) % 64) * 2);
-              ptx::mma_ss(d, ptx::desc_add(q_desc[t], off), ptx::desc_add(kd, off), idesc_s,
+              ptx::mma_ss(d, ptx::desc_add(q_desc, off), ptx::desc_add(kd, off), idesc_s,
                           s > 0 ? 1u : 0u);
             } else {
               const uint32_t off = (uint32_t)((s * 16 - QK::full * 64) * 2);
-              ptx::mma_ss(d, ptx::desc_add(q_desc_tail[t], off), ptx::desc_add(kd_tail, off),
+              ptx::mma_ss(d, ptx::desc_add(q_desc_tail, off), ptx::desc_add(kd_tail, off),
                           idesc_s, s > 0 ? 1u : 0u);
             }
           }
@@ -572,11 +594,15 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           const WorkItem w = decode_item(it, args, s_prefix, s_sorted);
           if (w.n_kv == 0) continue;
           const bool mine = t < w.n_qt;
+          const int qb = 2 * (C::q_pairs == 2 ? (int)(item_n & 1) : 0) + t;  // Q buffer
+          ++item_n;
           if (mine) {
             issued_any = true;
-            ok = wait_single(ptx::smem_u32(&cb->q_full[t]), qn & 1, abort_flag, args.status);
-            ++qn;
+            ok = wait_single(ptx::smem_u32(&cb->q_full[qb]), (q_par >> qb) & 1, abort_flag,
+                             args.status);
+            q_par ^= 1u << qb;
             if (!ok) break;
+            set_q(qb);
           }
           // Prologue: S_t(0).
           ok = wait_single(ptx::smem_u32(&cb->kv_full[slot]), phase, abort_flag, args.status);
@@ -588,7 +614,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             ptx::mma_commit(ptx::smem_u32(&cb->s_full[t]));
           }
           pass_turn();
-          if (mine && w.n_kv == 1) ptx::mma_commit(ptx::smem_u32(&cb->q_free[t]));
+          if (mine && w.n_kv == 1) ptx::mma_commit(ptx::smem_u32(&cb->q_free[qb]));
           ptx::mma_commit(ptx::smem_u32(&cb->kv_free[slot]));
           if (++slot == NS) { slot = 0; phase ^= 1; }
           for (int j = 0; j < w.n_kv && ok; ++j) {
@@ -633,7 +659,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             // would otherwise delay the other query tile's MMAs).
             pass_turn();
             if (has_next) {
-              if (mine && j + 2 == w.n_kv) ptx::mma_commit(ptx::smem_u32(&cb->q_free[t]));
+              if (mine && j + 2 == w.n_kv) ptx::mma_commit(ptx::smem_u32(&cb->q_free[qb]));
               ptx::mma_commit(ptx::smem_u32(&cb->kv_free[kslot]));
             }
             ptx::mma_commit(ptx::smem_u32(&cb->kv_free[vslot]));
@@ -838,7 +864,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
 template <int D_QK, int D_V>
 inline size_t varlen_smem_bytes(int batch) {
   using C = VarlenCfg<D_QK, D_V>;
-  return (size_t)1024 + 2 * C::q_tile_bytes + (size_t)C::nstage * C::slot_bytes +
+  return (size_t)1024 + 2 * C::q_pairs * C::q_tile_bytes + (size_t)C::nstage * C::slot_bytes +
          sizeof(VarlenBarriers) + 8 * (size_t)(batch + 1) + 4 * kVarlenThreads + 16;
 }
 
