@@ -3,8 +3,9 @@
 // One persistent CTA per SM walks a static, longest-first list of work items.
 // A work item is (sequence, head, pair of 128-row query tiles).  Per item:
 //
-//   producer warp   TMA: Q tiles once, then K_j, V_j tiles into a ring of
-//                   shared-memory slots guarded by mbarriers.
+//   producer warp   TMA: Q tiles once, then K_j and V_j tiles into two rings
+//                   of shared-memory slots (K ring, V ring) guarded by
+//                   mbarriers.
 //   MMA warps 9/10  one elected thread per query tile t issues tcgen05.mma:
 //                     S_t = Q_t K_jᵀ          (SS form, fp32 accumulator in TMEM)
 //                     O_t += P_t V_j          (TS form, P read from TMEM)
@@ -22,7 +23,7 @@
 //                   exp2, lazy O rescale (threshold kRescaleLog2), writes P_t
 //                   as bf16 into the S_t columns, and at the end normalises
 //                   O_t and stores O and the LSE.  Where d_v + 16 <= 128, P V
-//                   also produces the row sums: every ring slot ends in a
+//                   also produces the row sums: every V slot ends in a
 //                   16-wide V atom whose column 0 is ones, so O column d_v
 //                   accumulates sum_k P (rescaled with O); the fp32 sum is then
 //                   only kept when the LSE is returned.
@@ -30,8 +31,8 @@
 // TMEM (512 columns x 128 lanes x 32 bit):
 //   [  0,128) S_0 / P_0   [128,256) S_1 / P_1   [256,384) O_0   [384,512) O_1
 //
-// Shared memory: Q_0, Q_1 tiles, NSTAGE ring slots (each holds one K or one V
-// tile), mbarriers, and the work list.  Q and K tiles are column chunks of
+// Shared memory: one or two pairs of Q tiles, the K ring, the V ring,
+// mbarriers, and the work list.  Q and K tiles are column chunks of
 // the head dimension, 64 bf16 wide with the 128-byte swizzle (or one narrower
 // tail chunk with the 32/64-byte swizzle); V tiles are atoms of 16, 32 or 64
 // columns (v_atom_width).  Each is both the TMA box layout and the UMMA
@@ -68,7 +69,7 @@ constexpr int kRowsPerItem = 2 * kBM; // two query tiles per work item
 constexpr int kMaxBatch = 1024;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold, log2 units
 constexpr int kSmemBudget = 232448;   // 227 KB opt-in per CTA
-constexpr int kBarrierBytes = 320;    // VarlenBarriers, reserved in the smem budget
+constexpr int kBarrierBytes = 448;    // VarlenBarriers, reserved in the smem budget
 
 constexpr unsigned int kStatusTimeout = 1u;
 
@@ -121,7 +122,7 @@ struct VarlenCfg {
   static constexpr int q_tile_bytes = QK::tile_bytes(kBM);
   static constexpr int k_tile_bytes = QK::tile_bytes(kBN);
   // Row sums on the tensor core: when d_v + 16 fits the 128-column O region,
-  // each ring slot carries one more 16-wide V atom whose first column is all
+  // each V slot carries one more 16-wide V atom whose first column is all
   // ones (written once at kernel start), so P V also accumulates sum_k P[r, k]
   // into O column d_v, rescaled together with O.
   static constexpr bool sum_col = v_sum_column(D_V);
@@ -135,29 +136,37 @@ struct VarlenCfg {
   static constexpr int v_tile_bytes = v_data_atoms * v_atom_bytes;  // TMA bytes per V tile
   static constexpr int pv_n = VD::padded + (sum_col ? 16 : 0);
   static constexpr int v_region_bytes = v_atoms * v_atom_bytes;
-  static_assert(!sum_col || k_tile_bytes <= v_tile_bytes,
-                "a K tile would overwrite the ones atom of its slot");
-  static constexpr int slot_bytes =
-      ((k_tile_bytes > v_region_bytes ? k_tile_bytes : v_region_bytes) + 1023) / 1024 * 1024;
+  // K and V tiles live in two rings with their own slot sizes (a V slot
+  // also carries the ones atom).
+  static constexpr int k_slot_bytes = (k_tile_bytes + 1023) / 1024 * 1024;
+  static constexpr int v_slot_bytes = (v_region_bytes + 1023) / 1024 * 1024;
   static constexpr int sched_bytes_max = 8 * (kMaxBatch + 1) + 4 * kVarlenThreads;
-  // Ring slots that fit next to `pairs` pairs of Q tiles.
-  static constexpr int ring_fit(int pairs) {
-    return (kSmemBudget - (1024 /*align*/ + pairs * 2 * q_tile_bytes + kBarrierBytes) -
-            sched_bytes_max) / slot_bytes;
+  // Shared memory left for the rings next to `pairs` pairs of Q tiles.
+  static constexpr int ring_bytes(int pairs) {
+    return kSmemBudget - (1024 /*align*/ + pairs * 2 * q_tile_bytes + kBarrierBytes) -
+           sched_bytes_max;
+  }
+  static constexpr int min_(int a, int b) { return a < b ? a : b; }
+  // Equal K and V slot counts, at most 8 each.
+  static constexpr int pairs_fit(int pairs) {
+    return min_(8, ring_bytes(pairs) / (k_slot_bytes + v_slot_bytes));
   }
   // Two pairs of Q buffers, used by alternate work items, so that the next
   // item's Q loads while the current item runs (a short sequence's item is
   // only a few KV steps long, and its Q would otherwise wait for the
-  // current item's last S); only where six ring slots still fit.
-  static constexpr int q_pairs = ring_fit(2) >= 6 ? 2 : 1;
-  static constexpr int nstage_fit = ring_fit(q_pairs);
-  static constexpr int nstage = nstage_fit > 8 ? 8 : nstage_fit;
-  static_assert(nstage >= 2, "shared memory too small for two ring slots");
+  // current item's last S); only where three K and three V slots still fit.
+  static constexpr int q_pairs = pairs_fit(2) >= 3 ? 2 : 1;
+  static constexpr int nk = pairs_fit(q_pairs);
+  // One more V slot where the rest allows: a KV step needs V_j first, and
+  // V_{j+1} can then load while P V_j still reads V_j.
+  static constexpr int nv = min_(8, nk + ((ring_bytes(q_pairs) - nk * (k_slot_bytes + v_slot_bytes)) /
+                                          v_slot_bytes > 0 ? 1 : 0));
+  static_assert(nk >= 1 && nv >= 2, "shared memory too small for the K and V rings");
   static_assert(pv_n <= 128, "O accumulator wider than its TMEM region");
   // Issue order between the two query tiles' MMA groups.  Strict turns
   // (ping-pong) for d_qk == d_v, where a group is short and free-running
   // issuers fall into lockstep (measured: ViT d80 0.57 vs 0.67 ms); free
-  // running for d_qk > d_v (MLA 192/128: long S groups, a two-slot ring),
+  // running for d_qk > d_v (MLA 192/128: long S groups, one K slot),
   // where turns cost more than they save (causal 4 x 4096: 794 vs 699
   // TFLOP/s).
   static constexpr bool turns = D_QK == D_V;
@@ -195,12 +204,24 @@ struct alignas(8) VarlenBarriers {
   uint64_t o_free[2];
   uint64_t drain;
   uint64_t turn[2];  // issuer t may issue its next group
-  uint64_t kv_full[8];
-  uint64_t kv_free[8];
+  uint64_t k_full[8];   // K ring slot landed
+  uint64_t k_free[8];   // K ring slot released (one arrival per issuer)
+  uint64_t v_full[8];
+  uint64_t v_free[8];
   uint32_t tmem_base;
   volatile int abort_flag;
 };
 static_assert(sizeof(VarlenBarriers) <= kBarrierBytes, "barrier block larger than reserved");
+
+// Slot of the n-th tile loaded into a ring of Size slots (its fill parity is
+// (n / Size) & 1).  A one-slot ring's (d_qk = 192) constant slot is hidden
+// from the optimiser, which otherwise makes ptxas spill registers.
+template <int Size>
+__device__ __forceinline__ uint32_t ring_slot(uint32_t n) {
+  uint32_t s = n % (uint32_t)Size;
+  if (Size == 1) asm volatile("" : "+r"(s));
+  return s;
+}
 
 struct WorkItem {
   int q_start, k_start, lq, lk, head, kv_head, row0, n_qt, tile_lo, n_kv;
@@ -366,15 +387,16 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
   using C = VarlenCfg<D_QK, D_V>;
   using QK = typename C::QK;
   using VD = typename C::VD;
-  constexpr int NS = C::nstage;
+  constexpr int NK = C::nk, NV = C::nv;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // Q tile t of buffer pair p at smem + (2p + t) * q_tile_bytes.
   uint8_t* const q_base = smem;
-  uint8_t* ring = smem + 2 * C::q_pairs * C::q_tile_bytes;
-  VarlenBarriers* cb = reinterpret_cast<VarlenBarriers*>(ring + NS * C::slot_bytes);
+  uint8_t* k_ring = smem + 2 * C::q_pairs * C::q_tile_bytes;
+  uint8_t* v_ring = k_ring + NK * C::k_slot_bytes;
+  VarlenBarriers* cb = reinterpret_cast<VarlenBarriers*>(v_ring + NV * C::v_slot_bytes);
   int* s_prefix = reinterpret_cast<int*>(cb + 1);
   int* s_sorted = s_prefix + (args.batch + 1);
   int* s_part = s_sorted + args.batch;
@@ -398,9 +420,13 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     ptx::mbar_init(ptx::smem_u32(&cb->drain), 2);
     ptx::mbar_init(ptx::smem_u32(&cb->turn[0]), 1);
     ptx::mbar_init(ptx::smem_u32(&cb->turn[1]), 1);
-    for (int s = 0; s < NS; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&cb->kv_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&cb->kv_free[s]), 2);  // one release per issuer
+    for (int s = 0; s < NK; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&cb->k_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&cb->k_free[s]), 2);  // one release per issuer
+    }
+    for (int s = 0; s < NV; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&cb->v_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&cb->v_free[s]), 2);
     }
     cb->abort_flag = 0;
     ptx::fence_mbar_init();
@@ -421,13 +447,13 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
   if constexpr (C::sum_col) {
     // The ones atom after each slot's V data atoms: 128 rows of 32 bytes in
     // the 32-byte swizzle (the 16-byte half holding column 0 is swapped on
-    // rows with bit 2 set), column 0 = bf16 1.0, the rest 0.  Neither K
-    // (at most v_tile_bytes) nor V loads reach it.
+    // rows with bit 2 set), column 0 = bf16 1.0, the rest 0.  V loads stop
+    // before it.
     constexpr int kUnits = C::v_atom_bytes / 16;  // 16-byte units per atom
-    for (int e = tid; e < NS * kUnits; e += kVarlenThreads) {
+    for (int e = tid; e < NV * kUnits; e += kVarlenThreads) {
       const int slot = e / kUnits, u = e - slot * kUnits;
       const int row = u >> 1, half = u & 1;
-      uint4* dst = reinterpret_cast<uint4*>(ring + slot * C::slot_bytes + C::v_tile_bytes) + u;
+      uint4* dst = reinterpret_cast<uint4*>(v_ring + slot * C::v_slot_bytes + C::v_tile_bytes) + u;
       *dst = make_uint4(half == ((row >> 2) & 1) ? 0x3F80u : 0u, 0u, 0u, 0u);
     }
     ptx::fence_proxy_async_smem();  // read by the tensor core
@@ -448,9 +474,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         // phases consumed, of the Q loads issued, and whether any was issued.
         uint32_t qf_par = 0, qi_par = 0, qi_any = 0;
         uint32_t item_n = 0;  // items with KV tiles so far (selects the pair)
-        int slot = 0;
-        uint32_t phase = 0;
-        uint32_t slot_issued[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        // Tiles loaded into each ring so far: tile n goes to slot n % size,
+        // fill parity (n / size) & 1.
+        uint32_t kn = 0, vn = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < total_items && ok; it += gridDim.x) {
           const WorkItem w = decode_item(it, args, s_prefix, s_sorted);
@@ -477,28 +503,36 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           }
           for (int j = 0; j < w.n_kv && ok; ++j) {
             const int krow = w.k_start + (w.tile_lo + j) * kBN;
-            for (int kind = 0; kind < 2; ++kind) {  // 0: K tile, 1: V tile
-              ok = wait_single(ptx::smem_u32(&cb->kv_free[slot]), phase ^ 1, abort_flag,
-                               args.status);
-              if (!ok) break;
-              const uint32_t bar = ptx::smem_u32(&cb->kv_full[slot]);
-              uint8_t* dst = ring + slot * C::slot_bytes;
-              if (kind == 0) {
-                ptx::mbar_arrive_expect_tx(bar, C::k_tile_bytes);
+            // K_j into the K ring.
+            const uint32_t ks = ring_slot<NK>(kn);
+            ok = wait_single(ptx::smem_u32(&cb->k_free[ks]), ((kn / NK) & 1) ^ 1, abort_flag,
+                             args.status);
+            if (!ok) break;
+            {
+              const uint32_t bar = ptx::smem_u32(&cb->k_full[ks]);
+              uint8_t* dst = k_ring + ks * C::k_slot_bytes;
+              ptx::mbar_arrive_expect_tx(bar, C::k_tile_bytes);
 #pragma unroll
-                for (int c = 0; c < QK::chunks; ++c)
-                  ptx::tma_load_3d(ptx::smem_u32(dst + QK::chunk_off(c, kBN)),
-                                   c < QK::full ? &maps.k_full : &maps.k_tail, bar, c * 64,
-                                   w.kv_head, krow);
-              } else {
-                ptx::mbar_arrive_expect_tx(bar, C::v_tile_bytes);
+              for (int c = 0; c < QK::chunks; ++c)
+                ptx::tma_load_3d(ptx::smem_u32(dst + QK::chunk_off(c, kBN)),
+                                 c < QK::full ? &maps.k_full : &maps.k_tail, bar, c * 64,
+                                 w.kv_head, krow);
+              ++kn;
+            }
+            // V_j into the V ring.
+            const uint32_t vs = ring_slot<NV>(vn);
+            ok = wait_single(ptx::smem_u32(&cb->v_free[vs]), ((vn / NV) & 1) ^ 1, abort_flag,
+                             args.status);
+            if (!ok) break;
+            {
+              const uint32_t bar = ptx::smem_u32(&cb->v_full[vs]);
+              uint8_t* dst = v_ring + vs * C::v_slot_bytes;
+              ptx::mbar_arrive_expect_tx(bar, C::v_tile_bytes);
 #pragma unroll
-                for (int c = 0; c < C::v_data_atoms; ++c)
-                  ptx::tma_load_3d(ptx::smem_u32(dst + c * C::v_atom_bytes), &maps.v_full, bar,
-                                   c * C::v_atom, w.kv_head, krow);
-              }
-              ++slot_issued[slot];
-              if (++slot == NS) { slot = 0; phase ^= 1; }
+              for (int c = 0; c < C::v_data_atoms; ++c)
+                ptx::tma_load_3d(ptx::smem_u32(dst + c * C::v_atom_bytes), &maps.v_full, bar,
+                                 c * C::v_atom, w.kv_head, krow);
+              ++vn;
             }
           }
         }
@@ -508,10 +542,13 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             if ((qi_any >> b) & 1)
               wait_single(ptx::smem_u32(&cb->q_full[b]), ((qi_par >> b) & 1) ^ 1, abort_flag,
                           args.status);
-          for (int s = 0; s < NS; ++s)
-            if (slot_issued[s])
-              wait_single(ptx::smem_u32(&cb->kv_full[s]), (slot_issued[s] - 1) & 1, abort_flag,
-                          args.status);
+          // Slot s was last filled by tile s + size * ((n - 1 - s) / size).
+          for (uint32_t s = 0; s < (uint32_t)NK && s < kn; ++s)
+            wait_single(ptx::smem_u32(&cb->k_full[s]), ((kn - 1 - s) / NK) & 1, abort_flag,
+                        args.status);
+          for (uint32_t s = 0; s < (uint32_t)NV && s < vn; ++s)
+            wait_single(ptx::smem_u32(&cb->v_full[s]), ((vn - 1 - s) / NV) & 1, abort_flag,
+                        args.status);
         }
       }
       __syncwarp();
@@ -534,8 +571,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           if (C::turns) ptx::mbar_arrive(ptx::smem_u32(&cb->turn[t ^ 1]));
           ++groups;
         };
-        int slot = 0;
-        uint32_t phase = 0;
+        uint32_t kn = 0, vn = 0;  // tiles consumed from each ring
         bool ok = true;
         bool issued_any = false;
 
@@ -605,23 +641,28 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             set_q(qb);
           }
           // Prologue: S_t(0).
-          ok = wait_single(ptx::smem_u32(&cb->kv_full[slot]), phase, abort_flag, args.status);
-          if (ok) ok = take_turn();
-          if (!ok) break;
-          ptx::tc_fence_after();
-          if (mine) {
-            issue_s(ring + slot * C::slot_bytes);
-            ptx::mma_commit(ptx::smem_u32(&cb->s_full[t]));
-          }
-          pass_turn();
-          if (mine && w.n_kv == 1) ptx::mma_commit(ptx::smem_u32(&cb->q_free[qb]));
-          ptx::mma_commit(ptx::smem_u32(&cb->kv_free[slot]));
-          if (++slot == NS) { slot = 0; phase ^= 1; }
-          for (int j = 0; j < w.n_kv && ok; ++j) {
-            const int vslot = slot;
-            ok = wait_single(ptx::smem_u32(&cb->kv_full[vslot]), phase, abort_flag, args.status);
+          {
+            const uint32_t ks = ring_slot<NK>(kn);
+            ok = wait_single(ptx::smem_u32(&cb->k_full[ks]), (kn / NK) & 1, abort_flag,
+                             args.status);
+            if (ok) ok = take_turn();
             if (!ok) break;
-            if (++slot == NS) { slot = 0; phase ^= 1; }
+            ptx::tc_fence_after();
+            if (mine) {
+              issue_s(k_ring + ks * C::k_slot_bytes);
+              ptx::mma_commit(ptx::smem_u32(&cb->s_full[t]));
+            }
+            pass_turn();
+            if (mine && w.n_kv == 1) ptx::mma_commit(ptx::smem_u32(&cb->q_free[qb]));
+            ptx::mma_commit(ptx::smem_u32(&cb->k_free[ks]));
+            ++kn;
+          }
+          for (int j = 0; j < w.n_kv && ok; ++j) {
+            const uint32_t vs = ring_slot<NV>(vn);
+            ok = wait_single(ptx::smem_u32(&cb->v_full[vs]), (vn / NV) & 1, abort_flag,
+                             args.status);
+            if (!ok) break;
+            ++vn;
             const bool has_next = j + 1 < w.n_kv;
             ok = take_turn();
             if (!ok) break;
@@ -636,18 +677,17 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                 if (!ok) break;
               }
               ptx::tc_fence_after();
-              issue_pv(ring + vslot * C::slot_bytes, j == 0);
+              issue_pv(v_ring + vs * C::v_slot_bytes, j == 0);
             }
-            int kslot = -1;
+            const uint32_t ks = ring_slot<NK>(kn);
             if (has_next) {
-              kslot = slot;
-              ok = wait_single(ptx::smem_u32(&cb->kv_full[kslot]), phase, abort_flag,
+              ok = wait_single(ptx::smem_u32(&cb->k_full[ks]), (kn / NK) & 1, abort_flag,
                                args.status);
               if (!ok) break;
-              if (++slot == NS) { slot = 0; phase ^= 1; }
+              ++kn;
               if (mine) {
                 ptx::tc_fence_after();
-                issue_s(ring + kslot * C::slot_bytes);
+                issue_s(k_ring + ks * C::k_slot_bytes);
                 ptx::mma_commit(ptx::smem_u32(&cb->s_full[t]));
               }
             } else if (mine) {
@@ -660,9 +700,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             pass_turn();
             if (has_next) {
               if (mine && j + 2 == w.n_kv) ptx::mma_commit(ptx::smem_u32(&cb->q_free[qb]));
-              ptx::mma_commit(ptx::smem_u32(&cb->kv_free[kslot]));
+              ptx::mma_commit(ptx::smem_u32(&cb->k_free[ks]));
             }
-            ptx::mma_commit(ptx::smem_u32(&cb->kv_free[vslot]));
+            ptx::mma_commit(ptx::smem_u32(&cb->v_free[vs]));
           }
         }
         // Drain: every MMA issued by either issuer completes before TMEM is
@@ -864,7 +904,8 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
 template <int D_QK, int D_V>
 inline size_t varlen_smem_bytes(int batch) {
   using C = VarlenCfg<D_QK, D_V>;
-  return (size_t)1024 + 2 * C::q_pairs * C::q_tile_bytes + (size_t)C::nstage * C::slot_bytes +
+  return (size_t)1024 + 2 * C::q_pairs * C::q_tile_bytes + (size_t)C::nk * C::k_slot_bytes +
+         (size_t)C::nv * C::v_slot_bytes +
          sizeof(VarlenBarriers) + 8 * (size_t)(batch + 1) + 4 * kVarlenThreads + 16;
 }
 
