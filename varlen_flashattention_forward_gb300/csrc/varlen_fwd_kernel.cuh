@@ -223,6 +223,86 @@ __device__ __forceinline__ uint32_t ring_slot(uint32_t n) {
   return s;
 }
 
+// ------------------------------------------------------------ MMA groups
+// The MMA issuer warps run converged, and each group of MMAs is one asm
+// block in which elect.sync picks a lane and every tcgen05.mma is predicated
+// on it.  The same MMAs issued from a lane-0 branch share the SM
+// sub-partition's issue slots badly with the softmax warps there: measured
+// on one SM with two exp2/FMA warps beside the issuer, 85 clk per MMA from
+// the branch against 52 (the tensor-core rate of this group shape) this way.
+// Descriptor offsets are assembly-time constant expressions.
+
+// Block prologue: pa = accumulate, pz = overwrite, e = the elected lane.
+#define FA_GROUP_BEGIN                                                  \
+  "{\n\t.reg .pred e, pa, pz;\n\t.reg .b64 da, db;\n\t.reg .b32 ta;\n\t" \
+  "setp.ne.b32 pa, %7, 0;\n\tsetp.eq.b32 pz, %7, 0;\n\t"                \
+  "elect.sync _|e, 0xffffffff;\n\t"
+// S += Q K^T for one K=16 step: both descriptors advanced by OFF (16-byte
+// units).  Operands: %0 S columns, %1/%2 Q/K descriptors of the 64-wide
+// chunks, %3/%4 of the tail chunk, %5 instruction descriptor, %6 the
+// descriptor distance between 64-wide chunks, %7 the constant 1.
+#define FA_SS(QD, KD, OFF, ACC)                                            \
+  "add.s64 da, " QD ", " OFF ";\n\tadd.s64 db, " KD ", " OFF ";\n\t"       \
+  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, " ACC ";\n\t"
+// The four K=16 steps of 64-wide chunk C (128-byte swizzle: 32 bytes apart).
+#define FA_SS_CHUNK(C, ACC0)                                                  \
+  FA_SS("%1", "%2", "%6*" #C "+0", ACC0) FA_SS("%1", "%2", "%6*" #C "+2", "pa") \
+  FA_SS("%1", "%2", "%6*" #C "+4", "pa") FA_SS("%1", "%2", "%6*" #C "+6", "pa")
+#define FA_SS_TAIL(OFF) FA_SS("%3", "%4", OFF, "pa")
+
+// S_t = Q_t K_j^T over the padded head dimension: FULL 64-wide chunks and a
+// TAIL-wide (0, 16 or 32) last chunk, kBM == kBN so one offset addresses the
+// same chunk of Q and K.
+template <int FULL, int TAIL>
+__device__ __forceinline__ void issue_s_group(uint32_t d, uint64_t qd, uint64_t kd, uint64_t qdt,
+                                              uint64_t kdt, uint32_t idesc) {
+  constexpr uint32_t kChunk = (uint32_t)(kBN * 128) >> 4;  // chunk distance, 16-byte units
+#define FA_S_OPERANDS                                                                   \
+  ::"r"(d), "l"(qd), "l"(kd), "l"(qdt), "l"(kdt), "r"(idesc), "n"(kChunk), "r"(1u) \
+      : "memory"
+  if constexpr (FULL == 1 && TAIL == 0) {
+    asm volatile(FA_GROUP_BEGIN FA_SS_CHUNK(0, "pz") "}\n" FA_S_OPERANDS);
+  } else if constexpr (FULL == 1 && TAIL == 16) {
+    asm volatile(FA_GROUP_BEGIN FA_SS_CHUNK(0, "pz") FA_SS_TAIL("0") "}\n" FA_S_OPERANDS);
+  } else if constexpr (FULL == 1 && TAIL == 32) {
+    asm volatile(FA_GROUP_BEGIN FA_SS_CHUNK(0, "pz") FA_SS_TAIL("0") FA_SS_TAIL("2") "}\n"
+                 FA_S_OPERANDS);
+  } else if constexpr (FULL == 2 && TAIL == 0) {
+    asm volatile(FA_GROUP_BEGIN FA_SS_CHUNK(0, "pz") FA_SS_CHUNK(1, "pa") "}\n" FA_S_OPERANDS);
+  } else if constexpr (FULL == 3 && TAIL == 0) {
+    asm volatile(FA_GROUP_BEGIN FA_SS_CHUNK(0, "pz") FA_SS_CHUNK(1, "pa") FA_SS_CHUNK(2, "pa")
+                 "}\n" FA_S_OPERANDS);
+  } else {
+    static_assert(FULL < 0, "head dimension without an S issue group");
+  }
+#undef FA_S_OPERANDS
+}
+
+// O_t (+)= P_t V_j: eight K=16 steps over the 128 keys, P read from TMEM
+// (8 columns of packed bf16 pairs per step), V descriptor advanced by %6
+// (16-byte units) per step.  %4 = 0 overwrites O on the first step.
+#define FA_TS(S, ACC)                                                          \
+  "add.u32 ta, %1, 8*" S ";\n\tadd.s64 db, %2, %6*" S ";\n\t"                  \
+  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, " ACC ";\n\t"
+template <uint32_t kStepDesc>
+__device__ __forceinline__ void issue_pv_group(uint32_t o, uint32_t p, uint64_t vd, uint32_t idesc,
+                                               uint32_t acc_first) {
+  static_assert(kBN == 128, "eight K=16 steps per KV tile");
+  asm volatile(
+      "{\n\t.reg .pred e, pa, p0;\n\t.reg .b64 db;\n\t.reg .b32 ta;\n\t"
+      "setp.ne.b32 pa, %5, 0;\n\tsetp.ne.b32 p0, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      FA_TS("0", "p0") FA_TS("1", "pa") FA_TS("2", "pa") FA_TS("3", "pa")
+      FA_TS("4", "pa") FA_TS("5", "pa") FA_TS("6", "pa") FA_TS("7", "pa") "}\n"
+      ::"r"(o), "r"(p), "l"(vd), "r"(idesc), "r"(acc_first), "r"(1u), "n"(kStepDesc)
+      : "memory");
+}
+#undef FA_TS
+#undef FA_SS_TAIL
+#undef FA_SS_CHUNK
+#undef FA_SS
+#undef FA_GROUP_BEGIN
+
 struct WorkItem {
   int q_start, k_start, lq, lk, head, kv_head, row0, n_qt, tile_lo, n_kv;
 };
@@ -554,8 +634,10 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
       __syncwarp();
     } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
       // ---------------------------------------------------------- MMA issuers
-      if (lane == 0) {
-        const int t = warp - kMmaWarp;  // query tile this thread issues for
+      // The whole warp runs this converged (waits are warp-uniform); the
+      // MMAs, commits and arrives are done by one elected lane.
+      {
+        const int t = warp - kMmaWarp;  // query tile this warp issues for
         constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(kBM, kBN, false, false);
         uint32_t q_par = 0;   // bit b: parity of the q_full[b] phases consumed
         uint32_t item_n = 0;  // items with KV tiles so far (selects the Q pair)
@@ -565,20 +647,17 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         auto take_turn = [&]() -> bool {
           if (!C::turns || (t == 0 && groups == 0)) return true;
           const uint32_t par = (t == 0 ? groups - 1 : groups) & 1;
-          return wait_single(ptx::smem_u32(&cb->turn[t]), par, abort_flag, args.status);
+          return wait_warp(ptx::smem_u32(&cb->turn[t]), par, abort_flag, args.status);
         };
         auto pass_turn = [&]() {
-          if (C::turns) ptx::mbar_arrive(ptx::smem_u32(&cb->turn[t ^ 1]));
+          if (C::turns) ptx::mbar_arrive_elect(ptx::smem_u32(&cb->turn[t ^ 1]));
           ++groups;
         };
         uint32_t kn = 0, vn = 0;  // tiles consumed from each ring
         bool ok = true;
-        bool issued_any = false;
 
-        // Descriptors are built once per buffer; each MMA then only adds a
-        // constant byte offset to the start-address field (this thread
-        // shares its issue slots with two softmax warps, so the per-MMA
-        // instruction count matters).
+        // Descriptors are built once per buffer; the MMAs of a group add
+        // constant offsets to them.
         constexpr uint32_t kQkTailSbo = 8 * (QK::tail ? QK::tail : 16) * 2;
         constexpr uint32_t kQkTailLay = layout_for_width(QK::tail ? QK::tail : 16);
         // Descriptors of this issuer's Q tile in the current item's pair.
@@ -590,25 +669,12 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
               ptx::smem_desc(qa + QK::chunk_off(QK::full, kBM), 16, kQkTailSbo, kQkTailLay);
         };
         auto issue_s = [&](const uint8_t* kbuf) {
-          const uint32_t d = tmem + C::s_col(t);
           const uint32_t ka = ptx::smem_u32(kbuf);
           const uint64_t kd = ptx::smem_desc(ka, 16, 1024, ptx::kLayoutSw128);
           const uint64_t kd_tail =
               ptx::smem_desc(ka + QK::chunk_off(QK::full, kBN), 16, kQkTailSbo, kQkTailLay);
-#pragma unroll
-          for (int s = 0; s < QK::padded / 16; ++s) {
-            const int c = (s * 16) / 64;
-            if (c < QK::full) {
-              // kBM == kBN: the same offset addresses Q and K chunks.
-              const uint32_t off = (uint32_t)(QK::chunk_off(c, kBN) + ((s * 16) % 64) * 2);
-              ptx::mma_ss(d, ptx::desc_add(q_desc, off), ptx::desc_add(kd, off), idesc_s,
-                          s > 0 ? 1u : 0u);
-            } else {
-              const uint32_t off = (uint32_t)((s * 16 - QK::full * 64) * 2);
-              ptx::mma_ss(d, ptx::desc_add(q_desc_tail, off), ptx::desc_add(kd_tail, off),
-                          idesc_s, s > 0 ? 1u : 0u);
-            }
-          }
+          issue_s_group<QK::full, QK::tail>(tmem + C::s_col(t), q_desc, kd, q_desc_tail, kd_tail,
+                                            idesc_s);
         };
         auto issue_pv = [&](const uint8_t* vbuf, bool first) {
           // One MMA per 16 keys over all of d_v: MN-major B spanning
@@ -617,11 +683,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           constexpr uint32_t kRowBytes = C::v_atom * 2;
           const uint64_t vd = ptx::smem_desc(ptx::smem_u32(vbuf), C::v_atom_bytes, 8 * kRowBytes,
                                              layout_for_width(C::v_atom));
-          const uint32_t a0 = tmem + C::s_col(t);
-#pragma unroll
-          for (int s = 0; s < kBN / 16; ++s)
-            ptx::mma_ts(tmem + C::o_col(t), a0 + s * 8, ptx::desc_add(vd, s * 16 * kRowBytes),
-                        idesc_pv, (!first || s > 0) ? 1u : 0u);
+          // 16 keys = 16 rows of kRowBytes: kRowBytes 16-byte units per step.
+          issue_pv_group<kRowBytes>(tmem + C::o_col(t), tmem + C::s_col(t), vd, idesc_pv,
+                                    first ? 0u : 1u);
         };
         // Both issuers walk every KV tile of every item (to stay in phase on
         // the ring); an issuer whose tile is absent from the item only waits
@@ -633,9 +697,8 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           const int qb = 2 * (C::q_pairs == 2 ? (int)(item_n & 1) : 0) + t;  // Q buffer
           ++item_n;
           if (mine) {
-            issued_any = true;
-            ok = wait_single(ptx::smem_u32(&cb->q_full[qb]), (q_par >> qb) & 1, abort_flag,
-                             args.status);
+            ok = wait_warp(ptx::smem_u32(&cb->q_full[qb]), (q_par >> qb) & 1, abort_flag,
+                           args.status);
             q_par ^= 1u << qb;
             if (!ok) break;
             set_q(qb);
@@ -643,36 +706,36 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           // Prologue: S_t(0).
           {
             const uint32_t ks = ring_slot<NK>(kn);
-            ok = wait_single(ptx::smem_u32(&cb->k_full[ks]), (kn / NK) & 1, abort_flag,
-                             args.status);
+            ok = wait_warp(ptx::smem_u32(&cb->k_full[ks]), (kn / NK) & 1, abort_flag,
+                           args.status);
             if (ok) ok = take_turn();
             if (!ok) break;
             ptx::tc_fence_after();
             if (mine) {
               issue_s(k_ring + ks * C::k_slot_bytes);
-              ptx::mma_commit(ptx::smem_u32(&cb->s_full[t]));
+              ptx::mma_commit_elect(ptx::smem_u32(&cb->s_full[t]));
             }
             pass_turn();
-            if (mine && w.n_kv == 1) ptx::mma_commit(ptx::smem_u32(&cb->q_free[qb]));
-            ptx::mma_commit(ptx::smem_u32(&cb->k_free[ks]));
+            if (mine && w.n_kv == 1) ptx::mma_commit_elect(ptx::smem_u32(&cb->q_free[qb]));
+            ptx::mma_commit_elect(ptx::smem_u32(&cb->k_free[ks]));
             ++kn;
           }
           for (int j = 0; j < w.n_kv && ok; ++j) {
             const uint32_t vs = ring_slot<NV>(vn);
-            ok = wait_single(ptx::smem_u32(&cb->v_full[vs]), (vn / NV) & 1, abort_flag,
-                             args.status);
+            ok = wait_warp(ptx::smem_u32(&cb->v_full[vs]), (vn / NV) & 1, abort_flag,
+                           args.status);
             if (!ok) break;
             ++vn;
             const bool has_next = j + 1 < w.n_kv;
             ok = take_turn();
             if (!ok) break;
             if (mine) {
-              ok = wait_single(ptx::smem_u32(&cb->p_full[t]), pn & 1, abort_flag, args.status);
+              ok = wait_warp(ptx::smem_u32(&cb->p_full[t]), pn & 1, abort_flag, args.status);
               ++pn;
               if (!ok) break;
               if (j == 0) {
-                ok = wait_single(ptx::smem_u32(&cb->o_free[t]), (ofn & 1) ^ 1, abort_flag,
-                                 args.status);
+                ok = wait_warp(ptx::smem_u32(&cb->o_free[t]), (ofn & 1) ^ 1, abort_flag,
+                               args.status);
                 ++ofn;
                 if (!ok) break;
               }
@@ -681,17 +744,17 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             }
             const uint32_t ks = ring_slot<NK>(kn);
             if (has_next) {
-              ok = wait_single(ptx::smem_u32(&cb->k_full[ks]), (kn / NK) & 1, abort_flag,
-                               args.status);
+              ok = wait_warp(ptx::smem_u32(&cb->k_full[ks]), (kn / NK) & 1, abort_flag,
+                             args.status);
               if (!ok) break;
               ++kn;
               if (mine) {
                 ptx::tc_fence_after();
                 issue_s(k_ring + ks * C::k_slot_bytes);
-                ptx::mma_commit(ptx::smem_u32(&cb->s_full[t]));
+                ptx::mma_commit_elect(ptx::smem_u32(&cb->s_full[t]));
               }
             } else if (mine) {
-              ptx::mma_commit(ptx::smem_u32(&cb->o_full[t]));
+              ptx::mma_commit_elect(ptx::smem_u32(&cb->o_full[t]));
             }
             // The other issuer goes next; the commits that only release
             // buffers follow (a commit tracks this thread's MMAs alone, and
@@ -699,19 +762,18 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             // would otherwise delay the other query tile's MMAs).
             pass_turn();
             if (has_next) {
-              if (mine && j + 2 == w.n_kv) ptx::mma_commit(ptx::smem_u32(&cb->q_free[qb]));
-              ptx::mma_commit(ptx::smem_u32(&cb->k_free[ks]));
+              if (mine && j + 2 == w.n_kv)
+                ptx::mma_commit_elect(ptx::smem_u32(&cb->q_free[qb]));
+              ptx::mma_commit_elect(ptx::smem_u32(&cb->k_free[ks]));
             }
-            ptx::mma_commit(ptx::smem_u32(&cb->v_free[vs]));
+            ptx::mma_commit_elect(ptx::smem_u32(&cb->v_free[vs]));
           }
         }
         // Drain: every MMA issued by either issuer completes before TMEM is
         // freed (the barrier expects one arrival from each issuer).
-        (void)issued_any;
-        ptx::mma_commit(ptx::smem_u32(&cb->drain));
-        wait_single(ptx::smem_u32(&cb->drain), 0, abort_flag, args.status);
+        ptx::mma_commit_elect(ptx::smem_u32(&cb->drain));
+        wait_warp(ptx::smem_u32(&cb->drain), 0, abort_flag, args.status);
       }
-      __syncwarp();
     }
   } else {
     ptx::regs_inc<kSoftmaxRegs>();
