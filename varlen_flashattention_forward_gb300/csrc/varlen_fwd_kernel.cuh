@@ -22,11 +22,7 @@
 //                   masks only boundary tiles (software 3-input max there),
 //                   exp2, lazy O rescale (threshold kRescaleLog2), writes P_t
 //                   as bf16 into the S_t columns, and at the end normalises
-//                   O_t and stores O and the LSE.  Where d_v + 16 <= 128, P V
-//                   also produces the row sums: every V slot ends in a
-//                   16-wide V atom whose column 0 is ones, so O column d_v
-//                   accumulates sum_k P (rescaled with O); the fp32 sum is then
-//                   only kept when the LSE is returned.
+//                   O_t and stores O and the LSE.
 //
 // TMEM (512 columns x 128 lanes x 32 bit):
 //   [  0,128) S_0 / P_0   [128,256) S_1 / P_1   [256,384) O_0   [384,512) O_1
@@ -88,30 +84,17 @@ struct HeadDim {
   static constexpr int tile_bytes(int rows) { return rows * padded * 2; }
 };
 
-template <bool B>
-struct BoolTag {
-  static constexpr bool value = B;
-};
-
 __host__ __device__ constexpr uint32_t layout_for_width(int w) {
   return w == 64 ? ptx::kLayoutSw128 : (w == 32 ? ptx::kLayoutSw64 : ptx::kLayoutSw32);
 }
 
-// Whether P V also produces the row sums: d_v (rounded up to 16) plus a
-// 16-wide atom of ones fits the 128 TMEM columns of an O tile.
-__host__ __device__ constexpr bool v_sum_column(int d_v) {
-  return (d_v + 15) / 16 * 16 + 16 <= 128;
-}
-
-// Width (elements) of the swizzle atoms V is stored in: 16 when the ones
-// atom is appended (all atoms of one MMA operand share a layout), else the
-// widest of 64, 32 and 16 that divides d_v rounded up to 16.  Either way a V
-// tile holds no padding beyond that rounding (d_v = 80: five 16-wide atoms,
-// 20 KB per 128 keys, instead of two zero-filled 64-wide atoms, 32 KB).  The
-// host encodes the V tensor map with the same box width.
+// Width (elements) of the swizzle atoms V is stored in: the widest of 64,
+// 32 and 16 that divides d_v rounded up to 16, so that a V tile holds no
+// padding beyond that rounding (d_v = 80: five 16-wide atoms, 20 KB per 128
+// keys, instead of two zero-filled 64-wide atoms, 32 KB).  The host encodes
+// the V tensor map with the same box width.
 __host__ __device__ constexpr int v_atom_width(int d_v) {
-  return v_sum_column(d_v) ? 16
-         : ((d_v + 15) / 16 * 16) % 64 == 0 ? 64
+  return ((d_v + 15) / 16 * 16) % 64 == 0 ? 64
          : (((d_v + 15) / 16 * 16) % 32 == 0 ? 32 : 16);
 }
 
@@ -121,25 +104,16 @@ struct VarlenCfg {
   using VD = HeadDim<D_V>;
   static constexpr int q_tile_bytes = QK::tile_bytes(kBM);
   static constexpr int k_tile_bytes = QK::tile_bytes(kBN);
-  // Row sums on the tensor core: when d_v + 16 fits the 128-column O region,
-  // each V slot carries one more 16-wide V atom whose first column is all
-  // ones (written once at kernel start), so P V also accumulates sum_k P[r, k]
-  // into O column d_v, rescaled together with O.
-  static constexpr bool sum_col = v_sum_column(D_V);
   // V is stored MN-major as v_atoms atoms of v_atom columns (TMA zero-fills
-  // columns past d_v), so that P V is one MMA of N = pv_n per 16 keys: a
-  // tensor-core instruction costs about the same for any N up to 128.
+  // columns past d_v), so that P V is one MMA of N = pv_n per 16 keys.
   static constexpr int v_atom = v_atom_width(D_V);
-  static constexpr int v_data_atoms = VD::padded / v_atom;  // loaded by TMA
-  static constexpr int v_atoms = v_data_atoms + (sum_col ? 1 : 0);
+  static constexpr int v_atoms = VD::padded / v_atom;
   static constexpr int v_atom_bytes = kBN * v_atom * 2;
-  static constexpr int v_tile_bytes = v_data_atoms * v_atom_bytes;  // TMA bytes per V tile
-  static constexpr int pv_n = VD::padded + (sum_col ? 16 : 0);
-  static constexpr int v_region_bytes = v_atoms * v_atom_bytes;
-  // K and V tiles live in two rings with their own slot sizes (a V slot
-  // also carries the ones atom).
+  static constexpr int v_tile_bytes = v_atoms * v_atom_bytes;
+  static constexpr int pv_n = VD::padded;
+  // K and V tiles live in two rings with their own slot sizes.
   static constexpr int k_slot_bytes = (k_tile_bytes + 1023) / 1024 * 1024;
-  static constexpr int v_slot_bytes = (v_region_bytes + 1023) / 1024 * 1024;
+  static constexpr int v_slot_bytes = (v_tile_bytes + 1023) / 1024 * 1024;
   static constexpr int sched_bytes_max = 8 * (kMaxBatch + 1) + 4 * kVarlenThreads;
   // Shared memory left for the rings next to `pairs` pairs of Q tiles.
   static constexpr int ring_bytes(int pairs) {
@@ -524,20 +498,6 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     ptx::tmem_alloc(ptx::smem_u32(&cb->tmem_base), 512);
     ptx::tmem_relinquish();
   }
-  if constexpr (C::sum_col) {
-    // The ones atom after each slot's V data atoms: 128 rows of 32 bytes in
-    // the 32-byte swizzle (the 16-byte half holding column 0 is swapped on
-    // rows with bit 2 set), column 0 = bf16 1.0, the rest 0.  V loads stop
-    // before it.
-    constexpr int kUnits = C::v_atom_bytes / 16;  // 16-byte units per atom
-    for (int e = tid; e < NV * kUnits; e += kVarlenThreads) {
-      const int slot = e / kUnits, u = e - slot * kUnits;
-      const int row = u >> 1, half = u & 1;
-      uint4* dst = reinterpret_cast<uint4*>(v_ring + slot * C::v_slot_bytes + C::v_tile_bytes) + u;
-      *dst = make_uint4(half == ((row >> 2) & 1) ? 0x3F80u : 0u, 0u, 0u, 0u);
-    }
-    ptx::fence_proxy_async_smem();  // read by the tensor core
-  }
   build_work_list(args, s_prefix, s_sorted, s_part);  // ends with __syncthreads
   ptx::tc_fence_before();
   __syncthreads();
@@ -609,7 +569,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
               uint8_t* dst = v_ring + vs * C::v_slot_bytes;
               ptx::mbar_arrive_expect_tx(bar, C::v_tile_bytes);
 #pragma unroll
-              for (int c = 0; c < C::v_data_atoms; ++c)
+              for (int c = 0; c < C::v_atoms; ++c)
                 ptx::tma_load_3d(ptx::smem_u32(dst + c * C::v_atom_bytes), &maps.v_full, bar,
                                  c * C::v_atom, w.kv_head, krow);
               ++vn;
@@ -785,7 +745,6 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     const uint32_t o_addr = tmem + lane_base + C::o_col(t);
     const float sl2 = args.scale_log2;
     const float neg_inf = -__int_as_float(0x7f800000);
-    const bool want_lse = args.lse != nullptr;
     uint32_t sn = 0, on = 0;
     bool ok = true;
 
@@ -868,14 +827,11 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         const float base = (m_used == neg_inf) ? 0.f : m_used;
         // exp2(s * scale_log2 - base) with packed fp32x2 FMA / ADD (one
         // instruction per element pair), MUFU ex2 per element, and the fp32
-        // row sum in four packed accumulators when it is needed: always
-        // without the tensor-core sum column, else only for the LSE (the
-        // column sums the bf16-rounded P, which normalises O consistently but
-        // is a few 1e-3 off for a log-sum-exp over few keys).
+        // row sum in four packed accumulators.
         const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
         const uint64_t nbx2 = ptx::f2_pack(-base, -base);
         uint32_t pr[kBN / 2];
-        auto exp_tile = [&](auto with_sum) {
+        {
           uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
           for (int c = 0; c < kBN; c += 2) {
@@ -883,21 +839,14 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             ptx::f2_unpack(ptx::fma2(ptx::f2_pack(s[c], s[c + 1]), sl2x2, nbx2), x0, x1);
             const float p0 = ptx::ex2(x0);
             const float p1 = ptx::ex2(x1);
-            if constexpr (decltype(with_sum)::value)
-              ls2[(c >> 1) & 3] = ptx::add2(ls2[(c >> 1) & 3], ptx::f2_pack(p0, p1));
+            ls2[(c >> 1) & 3] = ptx::add2(ls2[(c >> 1) & 3], ptx::f2_pack(p0, p1));
             pr[c >> 1] = ptx::pack_bf16x2(p0, p1);
           }
-          if constexpr (decltype(with_sum)::value) {
-            float a0, a1, b0, b1;
-            ptx::f2_unpack(ptx::add2(ls2[0], ls2[1]), a0, a1);
-            ptx::f2_unpack(ptx::add2(ls2[2], ls2[3]), b0, b1);
-            l += (a0 + b0) + (a1 + b1);
-          }
-        };
-        if (!C::sum_col || want_lse)
-          exp_tile(BoolTag<true>{});
-        else
-          exp_tile(BoolTag<false>{});
+          float a0, a1, b0, b1;
+          ptx::f2_unpack(ptx::add2(ls2[0], ls2[1]), a0, a1);
+          ptx::f2_unpack(ptx::add2(ls2[2], ls2[3]), b0, b1);
+          l += (a0 + b0) + (a1 + b1);
+        }
 #pragma unroll
         for (int q = 0; q < kBN / 2; q += 32) ptx::tmem_st32(s_addr + q, pr + q);
         ptx::tmem_wait_st();
@@ -924,11 +873,8 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
 #pragma unroll
         for (int c = 0; c < C::pv_n; ++c) o[c] = 0u;
       }
-      // O is normalised by the sum of the bf16 P it was accumulated from
-      // (the tensor-core column) where there is one; the LSE uses the fp32 sum.
-      const float l_o = C::sum_col ? __uint_as_float(o[C::sum_col ? VD::padded : 0]) : l;
       if (row_valid) {
-        const float inv_l = l_o > 0.f ? 1.f / l_o : 0.f;
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
         const size_t tok = (size_t)(w.q_start + i);
         uint4* dst = reinterpret_cast<uint4*>(args.out +
                                               (tok * args.num_heads + w.head) * (size_t)D_V);
