@@ -671,61 +671,68 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             if (ok) ok = take_turn();
             if (!ok) break;
             ptx::tc_fence_after();
-            if (mine) {
-              issue_s(k_ring + ks * C::k_slot_bytes);
-              ptx::mma_commit_elect(ptx::smem_u32(&cb->s_full[t]));
-            }
+            if (mine) issue_s(k_ring + ks * C::k_slot_bytes);
             pass_turn();
-            if (mine && w.n_kv == 1) ptx::mma_commit_elect(ptx::smem_u32(&cb->q_free[qb]));
+            if (mine) {
+              ptx::mma_commit_elect(ptx::smem_u32(&cb->s_full[t]));
+              if (w.n_kv == 1) ptx::mma_commit_elect(ptx::smem_u32(&cb->q_free[qb]));
+            }
             ptx::mma_commit_elect(ptx::smem_u32(&cb->k_free[ks]));
             ++kn;
           }
           for (int j = 0; j < w.n_kv && ok; ++j) {
+            const bool has_next = j + 1 < w.n_kv;
+            // Operands and turn first: they are normally settled long before
+            // P_t(j) is, so the wait for P is the last thing before the MMAs.
+            // With a one-slot K ring, K_{j+1} only starts loading once both
+            // tiles' S(j) are done, so it is waited for after P V_j instead.
+            constexpr bool kEarlyK = NK > 1;
             const uint32_t vs = ring_slot<NV>(vn);
             ok = wait_warp(ptx::smem_u32(&cb->v_full[vs]), (vn / NV) & 1, abort_flag,
                            args.status);
             if (!ok) break;
             ++vn;
-            const bool has_next = j + 1 < w.n_kv;
+            const uint32_t ks = ring_slot<NK>(kn);
+            auto wait_k = [&]() -> bool {
+              const bool r = wait_warp(ptx::smem_u32(&cb->k_full[ks]), (kn / NK) & 1, abort_flag,
+                                       args.status);
+              ++kn;
+              return r;
+            };
+            if (kEarlyK && has_next) {
+              ok = wait_k();
+              if (!ok) break;
+            }
             ok = take_turn();
             if (!ok) break;
             if (mine) {
-              ok = wait_warp(ptx::smem_u32(&cb->p_full[t]), pn & 1, abort_flag, args.status);
-              ++pn;
-              if (!ok) break;
               if (j == 0) {
                 ok = wait_warp(ptx::smem_u32(&cb->o_free[t]), (ofn & 1) ^ 1, abort_flag,
                                args.status);
                 ++ofn;
                 if (!ok) break;
               }
+              ok = wait_warp(ptx::smem_u32(&cb->p_full[t]), pn & 1, abort_flag, args.status);
+              ++pn;
+              if (!ok) break;
               ptx::tc_fence_after();
               issue_pv(v_ring + vs * C::v_slot_bytes, j == 0);
             }
-            const uint32_t ks = ring_slot<NK>(kn);
-            if (has_next) {
-              ok = wait_warp(ptx::smem_u32(&cb->k_full[ks]), (kn / NK) & 1, abort_flag,
-                             args.status);
+            if (!kEarlyK && has_next) {
+              ok = wait_k();
               if (!ok) break;
-              ++kn;
-              if (mine) {
-                ptx::tc_fence_after();
-                issue_s(k_ring + ks * C::k_slot_bytes);
-                ptx::mma_commit_elect(ptx::smem_u32(&cb->s_full[t]));
-              }
-            } else if (mine) {
-              ptx::mma_commit_elect(ptx::smem_u32(&cb->o_full[t]));
+              ptx::tc_fence_after();
             }
-            // The other issuer goes next; the commits that only release
-            // buffers follow (a commit tracks this thread's MMAs alone, and
-            // with the tensor-core queue full each costs issue time that
+            if (mine && has_next) issue_s(k_ring + ks * C::k_slot_bytes);
+            // The other issuer goes next, then the commits (a commit tracks
+            // this thread's MMAs alone; issuing one costs the warp time that
             // would otherwise delay the other query tile's MMAs).
             pass_turn();
-            if (has_next) {
-              if (mine && j + 2 == w.n_kv)
-                ptx::mma_commit_elect(ptx::smem_u32(&cb->q_free[qb]));
-              ptx::mma_commit_elect(ptx::smem_u32(&cb->k_free[ks]));
+            if (mine) {
+              ptx::mma_commit_elect(ptx::smem_u32(has_next ? &cb->s_full[t] : &cb->o_full[t]));
+              if (j + 2 == w.n_kv) ptx::mma_commit_elect(ptx::smem_u32(&cb->q_free[qb]));
             }
+            if (has_next) ptx::mma_commit_elect(ptx::smem_u32(&cb->k_free[ks]));
             ptx::mma_commit_elect(ptx::smem_u32(&cb->v_free[vs]));
           }
         }
