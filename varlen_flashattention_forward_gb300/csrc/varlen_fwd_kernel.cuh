@@ -1,6 +1,7 @@
 // varlen_fwd_kernel.cuh -- variable-length attention forward for sm_103a.
 //
-// One persistent CTA per SM walks a static, longest-first list of work items.
+// One persistent CTA per SM walks its share of a static, longest-first list
+// of work items (dealt in snake order, snake_item).
 // A work item is (sequence, head, pair of 128-row query tiles).  Per item:
 //
 //   producer warp   TMA: Q tiles once, then K_j and V_j tiles into two rings
@@ -277,6 +278,17 @@ __device__ __forceinline__ void issue_pv_group(uint32_t o, uint32_t p, uint64_t 
 #undef FA_SS
 #undef FA_GROUP_BEGIN
 
+// Work items are sorted longest first and dealt to the CTAs in rounds of
+// gridDim.x, the direction reversed every other round, so that the CTAs that
+// take the longest item of one round take the shortest of the next.  For the
+// packed ViT mix (6 images, 256 to 9216 tokens, 16 heads) the busiest CTA then
+// carries 1.04x the mean work instead of 1.07x with a plain round robin;
+// causal 4 x 4096: 1.01x instead of 1.14x.
+__device__ __forceinline__ int snake_item(int round) {
+  const int g = (int)gridDim.x, b = (int)blockIdx.x;
+  return round * g + ((round & 1) ? g - 1 - b : b);
+}
+
 struct WorkItem {
   int q_start, k_start, lq, lk, head, kv_head, row0, n_qt, tile_lo, n_kv;
 };
@@ -518,7 +530,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         // fill parity (n / size) & 1.
         uint32_t kn = 0, vn = 0;
         bool ok = true;
-        for (int it = blockIdx.x; it < total_items && ok; it += gridDim.x) {
+        for (int r = 0; r * (int)gridDim.x < total_items && ok; ++r) {
+          const int it = snake_item(r);
+          if (it >= total_items) continue;
           const WorkItem w = decode_item(it, args, s_prefix, s_sorted);
           if (w.n_kv == 0) continue;
           const int pair = C::q_pairs == 2 ? (int)(item_n & 1) : 0;
@@ -650,7 +664,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         // Both issuers walk every KV tile of every item (to stay in phase on
         // the ring); an issuer whose tile is absent from the item only waits
         // and releases.
-        for (int it = blockIdx.x; it < total_items && ok; it += gridDim.x) {
+        for (int r = 0; r * (int)gridDim.x < total_items && ok; ++r) {
+          const int it = snake_item(r);
+          if (it >= total_items) continue;
           const WorkItem w = decode_item(it, args, s_prefix, s_sorted);
           if (w.n_kv == 0) continue;
           const bool mine = t < w.n_qt;
@@ -755,7 +771,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     uint32_t sn = 0, on = 0;
     bool ok = true;
 
-    for (int it = blockIdx.x; it < total_items && ok; it += gridDim.x) {
+    for (int r = 0; r * (int)gridDim.x < total_items && ok; ++r) {
+      const int it = snake_item(r);
+      if (it >= total_items) continue;
       const WorkItem w = decode_item(it, args, s_prefix, s_sorted);
       if (t >= w.n_qt) continue;
       const int i = w.row0 + t * kBM + row_in_tile;  // query row within the sequence
