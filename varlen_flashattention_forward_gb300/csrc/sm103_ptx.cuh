@@ -192,6 +192,30 @@ __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
       : "memory");
 }
 
+// Four K=16 steps D (+)= A * B with both operands in shared memory, issued by
+// one elected lane of a converged warp: step s uses a + s * kAStep and
+// b + s * kBStep (descriptor start-address units of 16 bytes); acc0 = 0 makes
+// the first step overwrite D.  A single asm block keeps the issue on the
+// uniform path (an MMA issued from a one-lane branch competes for issue slots
+// with the other warps of its SM sub-partition).
+template <uint32_t kAStep, uint32_t kBStep>
+__device__ __forceinline__ void mma_ss4_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred e, pa, p0;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 pa, %5, 0;\n\tsetp.ne.b32 p0, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
+      "add.s64 da, %1, %6*1;\n\tadd.s64 db, %2, %7*1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pa;\n\t"
+      "add.s64 da, %1, %6*2;\n\tadd.s64 db, %2, %7*2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pa;\n\t"
+      "add.s64 da, %1, %6*3;\n\tadd.s64 db, %2, %7*3;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pa;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc0), "r"(1u), "n"(kAStep), "n"(kBStep)
+      : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_elect(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"

@@ -359,7 +359,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // ------------------------------------------------------------ MMA issuers
     constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(64, NP, false, false);
     constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(128, NP, true, true);
-    if (warp == 8 && lane == 0) {
+    // Each issuer warp runs converged (warp-uniform waits); its MMAs go out
+    // four at a time from one elected lane, as do its commits.
+    if (warp == 8) {
       // Sᵀ(i) = R(i) Qᵀ into Sᵀ buffer i % 2, chunk by chunk as they land.
       const uint64_t qd = ptx::smem_desc(ptx::smem_u32(q_s), 16, 1024, ptx::kLayoutSw128);
       bool ok = true;
@@ -370,49 +372,49 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           if (seg > 0) {
             // Every S MMA that reads the current Q must be done before the
             // next segment's Q replaces it.
-            ptx::mma_commit(ptx::smem_u32(&cb->q_free));
-            ok = wait_single(ptx::smem_u32(&cb->q_free), (seg - 1) & 1, abort_flag, a.status);
+            ptx::mma_commit_elect(ptx::smem_u32(&cb->q_free));
+            ok = wait_warp(ptx::smem_u32(&cb->q_free), (seg - 1) & 1, abort_flag, a.status);
             if (!ok) break;
+            // (Segment 0's Q was issued at kernel start.)
+            if (lane == 0) {
+              const int unit = unit_of(i);
+              const int token = unit / a.groups;
+              const int head0 = (unit - token * a.groups) * 64;
+              ptx::mbar_arrive_expect_tx(ptx::smem_u32(&cb->q_full), 9 * NP * 128);
+              for (int c = 0; c < 9; ++c)
+                ptx::tma_load_3d(ptx::smem_u32(q_s + c * NP * 128), &q_map,
+                                 ptx::smem_u32(&cb->q_full), c * 64, head0, token);
+            }
+            __syncwarp();
           }
-          if (seg > 0) {  // segment 0's Q was issued at kernel start
-            const int unit = unit_of(i);
-            const int token = unit / a.groups;
-            const int head0 = (unit - token * a.groups) * 64;
-            ptx::mbar_arrive_expect_tx(ptx::smem_u32(&cb->q_full), 9 * NP * 128);
-            for (int c = 0; c < 9; ++c)
-              ptx::tma_load_3d(ptx::smem_u32(q_s + c * NP * 128), &q_map,
-                               ptx::smem_u32(&cb->q_full), c * 64, head0, token);
-          }
-          ok = wait_single(ptx::smem_u32(&cb->q_full), seg & 1, abort_flag, a.status);
+          ok = wait_warp(ptx::smem_u32(&cb->q_full), seg & 1, abort_flag, a.status);
           if (!ok) break;
           ++seg;
         }
         if (i >= 2) {
-          ok = wait_single(ptx::smem_u32(&cb->s_free[st]), ((i >> 1) - 1) & 1, abort_flag,
-                           a.status);
+          ok = wait_warp(ptx::smem_u32(&cb->s_free[st]), ((i >> 1) - 1) & 1, abort_flag,
+                         a.status);
           if (!ok) break;
         }
         const uint64_t rd = ptx::smem_desc(ptx::smem_u32(stage[st]), 16, 1024, ptx::kLayoutSw128);
         const uint32_t d = tmem + (uint32_t)(st * NP);
         for (int c = 0; c < kChunks && ok; ++c) {
-          ok = wait_single(ptx::smem_u32(&cb->r_full[st][c]), (i >> 1) & 1, abort_flag, a.status);
+          ok = wait_warp(ptx::smem_u32(&cb->r_full[st][c]), (i >> 1) & 1, abort_flag, a.status);
           if (!ok) break;
           // The gathered rows were written by cp.async (generic proxy); order
           // them before the tensor core's (async proxy) reads.
           ptx::fence_proxy_async_smem();
           ptx::tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            ptx::mma_ss(d, ptx::desc_add(rd, c * kChunkBytes + k * 32),
-                        ptx::desc_add(qd, c * NP * 128 + k * 32), idesc_s,
-                        (c > 0 || k > 0) ? 1u : 0u);
+          // Four K=16 steps over the chunk's 64 columns (32 bytes apart).
+          ptx::mma_ss4_elect<2, 2>(d, ptx::desc_add(rd, c * kChunkBytes),
+                                   ptx::desc_add(qd, c * NP * 128), idesc_s, c > 0 ? 1u : 0u);
         }
         if (!ok) break;
-        ptx::mma_commit(ptx::smem_u32(&cb->s_full[st]));
+        ptx::mma_commit_elect(ptx::smem_u32(&cb->s_full[st]));
       }
-      ptx::mma_commit(ptx::smem_u32(&cb->drain));
-      wait_single(ptx::smem_u32(&cb->drain), 0, abort_flag, a.status);
-    } else if (warp == 9 && lane == 0) {
+      ptx::mma_commit_elect(ptx::smem_u32(&cb->drain));
+      wait_warp(ptx::smem_u32(&cb->drain), 0, abort_flag, a.status);
+    } else if (warp == 9) {
       // Oᵀ += R(i)[:, 0:512]ᵀ Pᵀ(i), one 128-column m-tile at a time; each
       // m-tile's commit releases the chunks it was the last to read.  The
       // first PV of a segment overwrites Oᵀ, so it waits until the softmax
@@ -421,12 +423,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       int seg = 0;
       for (int i = 0; i < n && ok; ++i) {
         const int st = i & 1;
-        ok = wait_single(ptx::smem_u32(&cb->p_full[st]), (i >> 1) & 1, abort_flag, a.status);
+        ok = wait_warp(ptx::smem_u32(&cb->p_full[st]), (i >> 1) & 1, abort_flag, a.status);
         if (!ok) break;
         const bool first = seg_first(i);
         if (first) {
           if (seg > 0) {
-            ok = wait_single(ptx::smem_u32(&cb->o_free), (seg - 1) & 1, abort_flag, a.status);
+            ok = wait_warp(ptx::smem_u32(&cb->o_free), (seg - 1) & 1, abort_flag, a.status);
             if (!ok) break;
           }
           ++seg;
@@ -441,20 +443,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             ptx::smem_desc(ra + 8 * kChunkBytes, 8 * kPRowBytes, 8 * kPRowBytes, kSwP);
 #pragma unroll
         for (int m = 0; m < kPvGroups; ++m) {
-#pragma unroll
-          for (int k = 0; k < kDecodeKeys / 16; ++k)
-            ptx::mma_ss(tmem + 128u + (uint32_t)(m * NP),
-                        ptx::desc_add(ad, 2 * m * kChunkBytes + k * 16 * 128),
-                        ptx::desc_add(bd, k * 16 * kPRowBytes), idesc_o,
-                        (!first || k > 0) ? 1u : 0u);
-          ptx::mma_commit(ptx::smem_u32(&cb->r_free[st][m]));
+          // Four K=16 steps over the tile's 64 keys: 16 rows of R (128 bytes
+          // each) and 16 rows of Pᵀ per step.
+          ptx::mma_ss4_elect<16 * 128 / 16, 16 * kPRowBytes / 16>(
+              tmem + 128u + (uint32_t)(m * NP), ptx::desc_add(ad, 2 * m * kChunkBytes), bd,
+              idesc_o, first ? 0u : 1u);
+          ptx::mma_commit_elect(ptx::smem_u32(&cb->r_free[st][m]));
         }
-        ptx::mma_commit(ptx::smem_u32(&cb->pv_done[st]));
+        ptx::mma_commit_elect(ptx::smem_u32(&cb->pv_done[st]));
       }
-      ptx::mma_commit(ptx::smem_u32(&cb->drain));
-      wait_single(ptx::smem_u32(&cb->drain), 0, abort_flag, a.status);
+      ptx::mma_commit_elect(ptx::smem_u32(&cb->drain));
+      wait_warp(ptx::smem_u32(&cb->drain), 0, abort_flag, a.status);
     }
-    __syncwarp();
   } else {
     ptx::regs_inc<kDecodeSoftmaxRegs>();
     // ------------------------------------------------------------ softmax
