@@ -105,6 +105,26 @@ __device__ __forceinline__ uint64_t make_policy_evict_first() {
   return p;
 }
 
+// Bulk copy shared -> global of `bytes` (a multiple of 16, both addresses
+// 16-byte aligned), tracked in this thread's bulk async-group.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until every bulk group of this thread has finished reading its
+// shared-memory source (the buffer may then be reused).
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until every bulk group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Drops a 128-byte global line from L2 without writing it back: for scratch
 // data that has been read for the last time.
 __device__ __forceinline__ void discard_l2_line(const void* p) {
