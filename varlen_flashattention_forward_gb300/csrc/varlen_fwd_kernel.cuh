@@ -85,6 +85,11 @@ struct HeadDim {
   static constexpr int tile_bytes(int rows) { return rows * padded * 2; }
 };
 
+template <int V>
+struct IntTag {
+  static constexpr int value = V;
+};
+
 __host__ __device__ constexpr uint32_t layout_for_width(int w) {
   return w == 64 ? ptx::kLayoutSw128 : (w == 32 ? ptx::kLayoutSw64 : ptx::kLayoutSw32);
 }
@@ -153,6 +158,12 @@ struct VarlenCfg {
   // where turns cost more than they save (causal 4 x 4096: 794 vs 699
   // TFLOP/s).
   static constexpr bool turns = D_QK == D_V;
+  // P V is issued in two halves of 64 keys: the softmax hands over the
+  // first half of P before it computes the second, so that half of P V runs
+  // while the softmax is still busy (it shortens each tile's chain softmax ->
+  // P V -> S -> softmax by the half's tensor time).  Measured: ViT d80 +1 %;
+  // d_v = 128 (ViT d128, MLA) -3 %, where the extra handover costs more.
+  static constexpr bool split_pv = D_V <= 80;
   // TMEM columns of the S/P and O regions of query tile t.
   __host__ __device__ static constexpr uint32_t s_col(int t) { return 128u * (uint32_t)t; }
   __host__ __device__ static constexpr uint32_t o_col(int t) { return 256u + 128u * (uint32_t)t; }
@@ -183,6 +194,7 @@ struct alignas(8) VarlenBarriers {
   uint64_t q_free[4];
   uint64_t s_full[2];
   uint64_t p_full[2];
+  uint64_t p_half[2];  // P_t(j) keys 0..63 written (split_pv)
   uint64_t o_full[2];
   uint64_t o_free[2];
   uint64_t drain;
@@ -278,6 +290,21 @@ __device__ __forceinline__ void issue_pv_group(uint32_t o, uint32_t p, uint64_t 
       FA_TS("0", "p0") FA_TS("1", "pa") FA_TS("2", "pa") FA_TS("3", "pa")
       FA_TS("4", "pa") FA_TS("5", "pa") FA_TS("6", "pa") FA_TS("7", "pa") "}\n"
       ::"r"(o), "r"(p), "l"(vd), "r"(idesc), "r"(acc_first), "r"(1u), "n"(kStepDesc)
+      : "memory");
+}
+// Half of it: the four K=16 steps over keys [64 h, 64 h + 64) (P columns
+// 32 h .. 32 h + 32, V rows 64 h ..).
+template <uint32_t kStepDesc>
+__device__ __forceinline__ void issue_pv_half(uint32_t o, uint32_t p, uint64_t vd, uint32_t idesc,
+                                              uint32_t acc_first, int h) {
+  const uint32_t ph = p + (uint32_t)(h * 32);
+  const uint64_t vh = vd + (uint64_t)(h * 4 * kStepDesc);
+  asm volatile(
+      "{\n\t.reg .pred e, pa, p0;\n\t.reg .b64 db;\n\t.reg .b32 ta;\n\t"
+      "setp.ne.b32 pa, %5, 0;\n\tsetp.ne.b32 p0, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      FA_TS("0", "p0") FA_TS("1", "pa") FA_TS("2", "pa") FA_TS("3", "pa") "}\n"
+      ::"r"(o), "r"(ph), "l"(vh), "r"(idesc), "r"(acc_first), "r"(1u), "n"(kStepDesc)
       : "memory");
 }
 #undef FA_TS
@@ -488,6 +515,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(ptx::smem_u32(&cb->s_full[t]), 1);
       ptx::mbar_init(ptx::smem_u32(&cb->p_full[t]), kBM);
+      ptx::mbar_init(ptx::smem_u32(&cb->p_half[t]), kBM);
       ptx::mbar_init(ptx::smem_u32(&cb->o_full[t]), 1);
       ptx::mbar_init(ptx::smem_u32(&cb->o_free[t]), kBM);
     }
@@ -669,6 +697,14 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           issue_pv_group<kRowBytes>(tmem + C::o_col(t), tmem + C::s_col(t), vd, idesc_pv,
                                     first ? 0u : 1u);
         };
+        auto issue_pv_h = [&](const uint8_t* vbuf, bool first, int h) {
+          constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(kBM, C::pv_n, false, true);
+          constexpr uint32_t kRowBytes = C::v_atom * 2;
+          const uint64_t vd = ptx::smem_desc(ptx::smem_u32(vbuf), C::v_atom_bytes, 8 * kRowBytes,
+                                             layout_for_width(C::v_atom));
+          issue_pv_half<kRowBytes>(tmem + C::o_col(t), tmem + C::s_col(t), vd, idesc_pv,
+                                   first ? 0u : 1u, h);
+        };
         // Both issuers walk every KV tile of every item (to stay in phase on
         // the ring); an issuer whose tile is absent from the item only waits
         // and releases.
@@ -737,11 +773,20 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                 ++ofn;
                 if (!ok) break;
               }
+              if (C::split_pv) {
+                ok = wait_warp(ptx::smem_u32(&cb->p_half[t]), pn & 1, abort_flag, args.status);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                issue_pv_h(v_ring + vs * C::v_slot_bytes, j == 0, 0);
+              }
               ok = wait_warp(ptx::smem_u32(&cb->p_full[t]), pn & 1, abort_flag, args.status);
               ++pn;
               if (!ok) break;
               ptx::tc_fence_after();
-              issue_pv(v_ring + vs * C::v_slot_bytes, j == 0);
+              if (C::split_pv)
+                issue_pv_h(v_ring + vs * C::v_slot_bytes, false, 1);
+              else
+                issue_pv(v_ring + vs * C::v_slot_bytes, j == 0);
             }
             if (!kEarlyK && has_next) {
               ok = wait_k();
@@ -881,22 +926,35 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         uint32_t pr[kBN / 2];
         {
           uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
+          // Keys [c0, c0 + 64): exp2, row sum, P as bf16 pairs.
+          auto exp_half = [&](auto half) {
+            constexpr int c0 = decltype(half)::value * (kBN / 2);
 #pragma unroll
-          for (int c = 0; c < kBN; c += 2) {
-            float x0, x1;
-            ptx::f2_unpack(ptx::fma2(ptx::f2_pack(s[c], s[c + 1]), sl2x2, nbx2), x0, x1);
-            const float p0 = ptx::ex2(x0);
-            const float p1 = ptx::ex2(x1);
-            ls2[(c >> 1) & 3] = ptx::add2(ls2[(c >> 1) & 3], ptx::f2_pack(p0, p1));
-            pr[c >> 1] = ptx::pack_bf16x2(p0, p1);
+            for (int c = c0; c < c0 + kBN / 2; c += 2) {
+              float x0, x1;
+              ptx::f2_unpack(ptx::fma2(ptx::f2_pack(s[c], s[c + 1]), sl2x2, nbx2), x0, x1);
+              const float p0 = ptx::ex2(x0);
+              const float p1 = ptx::ex2(x1);
+              ls2[(c >> 1) & 3] = ptx::add2(ls2[(c >> 1) & 3], ptx::f2_pack(p0, p1));
+              pr[c >> 1] = ptx::pack_bf16x2(p0, p1);
+            }
+          };
+          exp_half(IntTag<0>{});
+          if (C::split_pv) {
+            // The first 64 keys' P goes out before the rest is computed.
+            ptx::tmem_st32(s_addr, pr);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(ptx::smem_u32(&cb->p_half[t]));
           }
+          exp_half(IntTag<1>{});
           float a0, a1, b0, b1;
           ptx::f2_unpack(ptx::add2(ls2[0], ls2[1]), a0, a1);
           ptx::f2_unpack(ptx::add2(ls2[2], ls2[3]), b0, b1);
           l += (a0 + b0) + (a1 + b1);
         }
 #pragma unroll
-        for (int q = 0; q < kBN / 2; q += 32) ptx::tmem_st32(s_addr + q, pr + q);
+        for (int q = C::split_pv ? 32 : 0; q < kBN / 2; q += 32) ptx::tmem_st32(s_addr + q, pr + q);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(ptx::smem_u32(&cb->p_full[t]));
