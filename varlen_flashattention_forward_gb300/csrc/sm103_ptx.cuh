@@ -105,6 +105,13 @@ __device__ __forceinline__ uint64_t make_policy_evict_first() {
   return p;
 }
 
+// 32-byte global store (dst 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // Bulk copy shared -> global of `bytes` (a multiple of 16, both addresses
 // 16-byte aligned), tracked in this thread's bulk async-group.
 __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
