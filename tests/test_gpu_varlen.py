@@ -134,6 +134,27 @@ def test_single_key_returns_v_exactly(cuda_device):
     assert torch.equal(out, v)
 
 
+@pytest.mark.parametrize("d", [80, 128])
+def test_output_only_16_byte_aligned(cuda_device, d):
+    # O rows are written by bulk copies (d80), 32-byte stores when the output
+    # is 32-byte aligned, and 16-byte stores otherwise: an output buffer that
+    # starts 16 bytes into an allocation takes the last path (d128) and the
+    # bulk-copy path with a 16-byte aligned destination (d80).
+    lens = [300, 129, 64]
+    q, k, v, cq, ck = make(lens, lens, 2, 2, d, d, seed=16)
+    dev = torch.device("cuda:0")
+    T, H = q.shape[0], q.shape[1]
+    big = torch.full((T * H * d + 8,), float("nan"), dtype=torch.bfloat16, device=dev)
+    out = big[8:].view(T, H, d)  # 16 bytes past a 256-byte aligned start
+    assert out.data_ptr() % 32 == 16
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    fa.fa_varlen_fwd(q.to(dev), k.to(dev), v.to(dev), cq.to(dev), ck.to(dev), 0, 0, d ** -0.5,
+                     True, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.isnan(big[:8].float()).all()  # nothing written before the output
+    compare(q, k, v, cq, ck, d ** -0.5, causal=True, out=out.cpu(), lse=lse.cpu())
+
+
 def test_bitwise_deterministic(cuda_device):
     w = workloads.tiny()
     lens = [3000, 50, 1200]
