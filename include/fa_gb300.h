@@ -11,8 +11,9 @@
  * gathered from a paged 576-wide latent cache.
  *
  * Conventions shared by every entry point
- *   - All tensors are caller-owned device buffers, C-contiguous, 16-byte
- *     aligned.  bf16 means IEEE bfloat16 bit patterns (2 bytes).
+ *   - All tensors are caller-owned device buffers, C-contiguous (except the
+ *     q/k/v views fa_varlen_fwd_strided takes), 16-byte aligned.  bf16 means
+ *     IEEE bfloat16 bit patterns (2 bytes).
  *   - Calls are asynchronous on `stream` (NULL = legacy default stream).  The
  *     library allocates no memory, performs no host<->device copy and never
  *     synchronises; it only encodes TMA descriptors on the host and launches.
@@ -108,6 +109,33 @@ fa_status fa_varlen_fwd(const void* q, const void* k, const void* v,
                         int max_seqlen_k, float softmax_scale, int causal,
                         int window_left, int window_right, void* out,
                         float* lse, fa_stream_t stream);
+
+/*
+ * fa_varlen_fwd_strided -- fa_varlen_fwd with q, k and v given as strided
+ * views: element (t, h, c) of q is at q + t * q_row_stride + h *
+ * q_head_stride + c, likewise for k and v; strides are in elements.  This is
+ * the v_stride of [flash_attn] (FA4MLAPrefillKernel.dispatch, the CompileKey's
+ * v_stride when V needs no padding): V read straight out of a combined
+ * [tokens, heads, nope + v] buffer, its rows num_heads * (nope + v_dim) and
+ * its heads nope + v_dim elements apart.
+ *
+ *   *_row_stride, *_head_stride  multiples of 8 (16 bytes), head stride >=
+ *                 the tensor's last dimension, row stride >= (heads - 1) *
+ *                 head stride + last dimension (views do not overlap
+ *                 themselves); the innermost dimension is contiguous.
+ *   all other arguments and errors as fa_varlen_fwd; a stride that breaks
+ *   these rules is FA_ERR_INVALID_ARG.  out and lse stay contiguous.
+ *   fa_varlen_fwd is this call with the contiguous strides
+ *   (num_heads * d, d).
+ */
+fa_status fa_varlen_fwd_strided(const void* q, long long q_row_stride, long long q_head_stride,
+                                const void* k, long long k_row_stride, long long k_head_stride,
+                                const void* v, long long v_row_stride, long long v_head_stride,
+                                const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                                int total_q, int total_k, int num_heads, int num_heads_k,
+                                int d_qk, int d_v, int max_seqlen_q, int max_seqlen_k,
+                                float softmax_scale, int causal, int window_left,
+                                int window_right, void* out, float* lse, fa_stream_t stream);
 
 /*
  * fa_sparse_mla_decode -- one query row per token attending over top-k rows

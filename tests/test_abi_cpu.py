@@ -83,6 +83,44 @@ def test_varlen_host_validation(lib, kw, expect):
     assert varlen(lib, **kw) == expect
 
 
+def varlen_strided(lib, **kw):
+    # V as the upper 64 columns of a combined [tokens, 4 heads, 128] buffer.
+    a = dict(q=P(0x1000), qr=4 * 64, qh=64, k=P(0x2000), kr=4 * 64, kh=64, v=P(0x3000),
+             vr=4 * 128, vh=128, cq=P(0x4000), ck=P(0x5000), batch=2, total_q=10, total_k=10,
+             H=4, Hk=4, dqk=64, dv=64, scale=0.125, causal=0, wl=-1, wr=-1, out=P(0x6000),
+             lse=None)
+    a.update(kw)
+    return lib.fa_varlen_fwd_strided(a["q"], a["qr"], a["qh"], a["k"], a["kr"], a["kh"], a["v"],
+                                     a["vr"], a["vh"], a["cq"], a["ck"], a["batch"],
+                                     a["total_q"], a["total_k"], a["H"], a["Hk"], a["dqk"],
+                                     a["dv"], 0, 0, a["scale"], a["causal"], a["wl"], a["wr"],
+                                     a["out"], a["lse"], None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(vh=60),                # head stride below the head dim
+    dict(vh=132),               # not a multiple of 8 elements (16 bytes)
+    dict(vr=3 * 128 + 63),      # rows overlap the last head
+    dict(kr=0),                 # zero stride
+    dict(qh=-64),               # negative stride
+    dict(qr=3 * 64 + 56),       # q rows overlap
+    dict(v=P(0x3008)),          # base not 16-byte aligned
+])
+def test_varlen_strided_host_validation(lib, kw):
+    assert varlen_strided(lib, **kw) == fa.FA_ERR_INVALID_ARG
+
+
+def test_varlen_strided_valid_views_pass_validation(lib):
+    """Valid strided views get past the host checks (then fail only for want
+    of a GPU, or launch when one is present)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert varlen_strided(lib) in (fa.FA_ERR_LAUNCH, fa.FA_ERR_ARCH)
+    # The contiguous strides are the plain entry point's.
+    assert varlen_strided(lib, vr=4 * 64, vh=64) in (fa.FA_ERR_LAUNCH, fa.FA_ERR_ARCH)
+
+
 def decode(lib, **kw):
     a = dict(q=P(0x1000), c=P(0x2000), pt=P(0x3000), ti=P(0x4000), T=4, H=64, topk=256,
              pages=100, maxp=16, scale=0.04, out=P(0x5000), lse=None, stream=None)

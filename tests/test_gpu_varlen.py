@@ -155,6 +155,33 @@ def test_output_only_16_byte_aligned(cuda_device, d):
     compare(q, k, v, cq, ck, d ** -0.5, causal=True, out=out.cpu(), lse=lse.cpu())
 
 
+@pytest.mark.parametrize("dqk,dv,H,Hk", [(128, 128, 4, 4), (192, 128, 4, 4), (80, 80, 4, 2)])
+def test_strided_views(cuda_device, dqk, dv, H, Hk):
+    # V (and K) read straight out of a combined [tokens, heads, nope + v]
+    # buffer, Q out of a wider buffer: row and head strides differ from the
+    # dense ones, and the result must not change.
+    lens_q, lens_k = [300, 129, 64], [300, 400, 64]
+    g = torch.Generator().manual_seed(17)
+    Tq, Tk = sum(lens_q), sum(lens_k)
+    qbuf = torch.randn(Tq, H, dqk + 64, generator=g).bfloat16()
+    kvbuf = torch.randn(Tk, Hk, dqk + dv, generator=g).bfloat16()
+    q, k, v = qbuf[:, :, :dqk], kvbuf[:, :, :dqk], kvbuf[:, :, dqk:]
+    cq, ck = cu(lens_q), cu(lens_k)
+    dev = torch.device("cuda:0")
+    qd, kvd = qbuf.to(dev), kvbuf.to(dev)
+    out, lse = fa.fa_varlen_fwd(qd[:, :, :dqk], kvd[:, :, :dqk], kvd[:, :, dqk:], cq.to(dev),
+                                ck.to(dev), 0, 0, dqk ** -0.5, True, return_lse=True)
+    torch.cuda.synchronize()
+    compare(q.contiguous(), k.contiguous(), v.contiguous(), cq, ck, dqk ** -0.5, causal=True,
+            out=out.cpu(), lse=lse.cpu())
+    # Bitwise the same as the dense call on copies.
+    out2, lse2 = fa.fa_varlen_fwd(qd[:, :, :dqk].contiguous(), kvd[:, :, :dqk].contiguous(),
+                                  kvd[:, :, dqk:].contiguous(), cq.to(dev), ck.to(dev), 0, 0,
+                                  dqk ** -0.5, True, return_lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), out2.cpu()) and torch.equal(lse.cpu(), lse2.cpu())
+
+
 def test_bitwise_deterministic(cuda_device):
     w = workloads.tiny()
     lens = [3000, 50, 1200]

@@ -35,8 +35,9 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
 
 # Exported C symbols (kept in sync with include/fa_gb300.h; a CPU test checks).
-EXPORTS = ("fa_varlen_fwd", "fa_sparse_mla_decode", "fa_sparse_mla_decode_noalloc",
-           "fa_merge_attn_states", "fa_get_device_status", "fa_status_string")
+EXPORTS = ("fa_varlen_fwd", "fa_varlen_fwd_strided", "fa_sparse_mla_decode",
+           "fa_sparse_mla_decode_noalloc", "fa_merge_attn_states", "fa_get_device_status",
+           "fa_status_string")
 
 _lib = None
 
@@ -61,6 +62,11 @@ def load_library():
     lib.fa_varlen_fwd.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, i32,
                                   i32, i32, i32, f32, i32, i32, i32, p, p, p]
     lib.fa_varlen_fwd.restype = i32
+    i64 = ctypes.c_longlong
+    lib.fa_varlen_fwd_strided.argtypes = [p, i64, i64, p, i64, i64, p, i64, i64, p, p, i32,
+                                          i32, i32, i32, i32, i32, i32, i32, i32, f32, i32,
+                                          i32, i32, p, p, p]
+    lib.fa_varlen_fwd_strided.restype = i32
     lib.fa_sparse_mla_decode.argtypes = [p, p, p, p, i32, i32, i32, i32, i32,
                                          f32, p, p, p]
     lib.fa_sparse_mla_decode.restype = i32
@@ -95,12 +101,17 @@ def _stream_ptr(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _check(t, name, dtype, ndim):
+def _check(t, name, dtype, ndim, view=False):
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
-    if not t.is_contiguous():
+    if view:
+        # A strided view is passed as (pointer, row stride, head stride); the
+        # library checks the strides, the innermost dimension must be dense.
+        if t.stride(-1) != 1:
+            raise ValueError(f"{name} must have a contiguous last dimension")
+    elif not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
 
 
@@ -113,12 +124,15 @@ def fa_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=0,
     q [total_q, H, d_qk], k [total_k, H_k, d_qk], v [total_k, H_k, d_v] bf16
     CUDA tensors; cu_seqlens_* int32 [batch+1] CUDA tensors.  Returns out
     [total_q, H, d_v] bf16, or (out, lse [H, total_q] fp32) if an lse buffer
-    is given or return_lse is set.
+    is given or return_lse is set.  q, k and v may be strided views with a
+    contiguous last dimension (for example V taken out of a combined
+    [tokens, heads, nope + v] buffer); they then go through
+    fa_varlen_fwd_strided.
     """
     import torch
     lib = load_library()
     for name, t in (("q", q), ("k", k), ("v", v)):
-        _check(t, name, torch.bfloat16, 3)
+        _check(t, name, torch.bfloat16, 3, view=True)
     _check(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
     _check(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
     total_q, H, d_qk = q.shape
@@ -138,12 +152,21 @@ def fa_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=0,
         lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
     if lse is not None:
         _check(lse, "lse", torch.float32, 2)
-    st = lib.fa_varlen_fwd(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
-        batch, total_q, total_k, H, H_k, d_qk, d_v, int(max_seqlen_q),
-        int(max_seqlen_k), float(softmax_scale), int(bool(causal)),
-        int(window_left), int(window_right), _ptr(out), _ptr(lse),
-        _stream_ptr(stream))
+    if q.is_contiguous() and k.is_contiguous() and v.is_contiguous():
+        st = lib.fa_varlen_fwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+            batch, total_q, total_k, H, H_k, d_qk, d_v, int(max_seqlen_q),
+            int(max_seqlen_k), float(softmax_scale), int(bool(causal)),
+            int(window_left), int(window_right), _ptr(out), _ptr(lse),
+            _stream_ptr(stream))
+    else:
+        st = lib.fa_varlen_fwd_strided(
+            _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
+            _ptr(v), v.stride(0), v.stride(1), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+            batch, total_q, total_k, H, H_k, d_qk, d_v, int(max_seqlen_q),
+            int(max_seqlen_k), float(softmax_scale), int(bool(causal)),
+            int(window_left), int(window_right), _ptr(out), _ptr(lse),
+            _stream_ptr(stream))
     if st != FA_OK:
         raise FaError(st, "fa_varlen_fwd")
     return (out, lse) if lse is not None else out

@@ -99,12 +99,13 @@ EncodeTiledFn encode_fn() {
 // {box_w, 1, box_rows}.  The swizzle matches the box width (64 -> 128 B,
 // 32 -> 64 B, 16 -> 32 B).  Elements past `dim` or `tokens` read as zero.
 bool encode_rows(CUtensorMap* m, const void* base, int dim, int heads, int tokens, int box_w,
-                 int box_rows) {
+                 int box_rows, long long head_stride, long long row_stride) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)dim, (cuuint64_t)heads,
                         (cuuint64_t)(tokens > 0 ? tokens : 1)};
-  cuuint64_t strides[2] = {(cuuint64_t)dim * 2, (cuuint64_t)heads * dim * 2};
+  // Strides in bytes of the head and token dimensions (elements are bf16).
+  cuuint64_t strides[2] = {(cuuint64_t)head_stride * 2, (cuuint64_t)row_stride * 2};
   cuuint32_t box[3] = {(cuuint32_t)box_w, 1u, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUtensorMapSwizzle swz = box_w == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
@@ -146,6 +147,20 @@ int tail_width(int d) { return ((d + 15) / 16 * 16) % 64; }
 
 }  // namespace
 
+namespace {
+
+// A strided [tokens, heads, dim] view: innermost dimension contiguous, head
+// and token strides multiples of 16 bytes, no element reachable two ways.
+bool valid_view(long long row_stride, long long head_stride, int heads, int dim) {
+  if (row_stride <= 0 || head_stride <= 0) return false;
+  if (row_stride % 8 != 0 || head_stride % 8 != 0) return false;
+  if (head_stride < dim) return false;
+  if (row_stride < (long long)(heads - 1) * head_stride + dim) return false;
+  return row_stride < (1ll << 37) && head_stride < (1ll << 37);  // TMA stride range
+}
+
+}  // namespace
+
 extern "C" fa_status fa_varlen_fwd(const void* q, const void* k, const void* v,
                                    const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
                                    int total_q, int total_k, int num_heads, int num_heads_k,
@@ -153,6 +168,20 @@ extern "C" fa_status fa_varlen_fwd(const void* q, const void* k, const void* v,
                                    float softmax_scale, int causal, int window_left,
                                    int window_right, void* out, float* lse,
                                    fa_stream_t stream) {
+  return fa_varlen_fwd_strided(
+      q, (long long)num_heads * d_qk, d_qk, k, (long long)num_heads_k * d_qk, d_qk, v,
+      (long long)num_heads_k * d_v, d_v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
+      num_heads, num_heads_k, d_qk, d_v, max_seqlen_q, max_seqlen_k, softmax_scale, causal,
+      window_left, window_right, out, lse, stream);
+}
+
+extern "C" fa_status fa_varlen_fwd_strided(
+    const void* q, long long q_row_stride, long long q_head_stride, const void* k,
+    long long k_row_stride, long long k_head_stride, const void* v, long long v_row_stride,
+    long long v_head_stride, const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+    int total_q, int total_k, int num_heads, int num_heads_k, int d_qk, int d_v,
+    int max_seqlen_q, int max_seqlen_k, float softmax_scale, int causal, int window_left,
+    int window_right, void* out, float* lse, fa_stream_t stream) {
   (void)max_seqlen_q;
   (void)max_seqlen_k;
   // ---- host validation (before any CUDA call)
@@ -177,6 +206,10 @@ extern "C" fa_status fa_varlen_fwd(const void* q, const void* k, const void* v,
   else if (d_qk == 128 && d_v == 128) launch = fa::launch_varlen_128_128;
   else if (d_qk == 192 && d_v == 128) launch = fa::launch_varlen_192_128;
   if (!launch) return FA_ERR_UNSUPPORTED;
+  if (!valid_view(q_row_stride, q_head_stride, num_heads, d_qk) ||
+      (total_k > 0 && (!valid_view(k_row_stride, k_head_stride, num_heads_k, d_qk) ||
+                       !valid_view(v_row_stride, v_head_stride, num_heads_k, d_v))))
+    return FA_ERR_INVALID_ARG;
   // Token indices are 32-bit in the kernel.
   if ((int64_t)total_q * num_heads > INT32_MAX || (int64_t)total_k * num_heads_k > INT32_MAX)
     return FA_ERR_UNSUPPORTED;
@@ -194,13 +227,19 @@ extern "C" fa_status fa_varlen_fwd(const void* q, const void* k, const void* v,
   const int kh = total_k > 0 ? num_heads_k : num_heads;
   const int vd = total_k > 0 ? d_v : d_qk;
   const int tk = total_k > 0 ? total_k : total_q;
+  const long long krs = total_k > 0 ? k_row_stride : q_row_stride;
+  const long long khs = total_k > 0 ? k_head_stride : q_head_stride;
+  const long long vrs = total_k > 0 ? v_row_stride : q_row_stride;
+  const long long vhs = total_k > 0 ? v_head_stride : q_head_stride;
   const int qt = tail_width(d_qk);
-  bool ok = encode_rows(&maps.q_full, q, d_qk, num_heads, total_q, 64, fa::kBM) &&
-            encode_rows(&maps.k_full, kb, d_qk, kh, tk, 64, fa::kBN) &&
-            encode_rows(&maps.v_full, vb, vd, kh, tk, fa::v_atom_width(vd), fa::kBN);
+  bool ok = encode_rows(&maps.q_full, q, d_qk, num_heads, total_q, 64, fa::kBM, q_head_stride,
+                        q_row_stride) &&
+            encode_rows(&maps.k_full, kb, d_qk, kh, tk, 64, fa::kBN, khs, krs) &&
+            encode_rows(&maps.v_full, vb, vd, kh, tk, fa::v_atom_width(vd), fa::kBN, vhs, vrs);
   if (ok && qt)
-    ok = encode_rows(&maps.q_tail, q, d_qk, num_heads, total_q, qt, fa::kBM) &&
-         encode_rows(&maps.k_tail, kb, d_qk, kh, tk, qt, fa::kBN);
+    ok = encode_rows(&maps.q_tail, q, d_qk, num_heads, total_q, qt, fa::kBM, q_head_stride,
+                     q_row_stride) &&
+         encode_rows(&maps.k_tail, kb, d_qk, kh, tk, qt, fa::kBN, khs, krs);
   if (!ok) return FA_ERR_LAUNCH;
 
   fa::VarlenArgs args;
