@@ -7,11 +7,12 @@
 //   producer warp   TMA: Q tiles once, then K_j and V_j tiles into two rings
 //                   of shared-memory slots (K ring, V ring) guarded by
 //                   mbarriers.
-//   MMA warps 9/10  one elected thread per query tile t issues tcgen05.mma:
+//   MMA warps 9/10  one warp per query tile t, running converged; an
+//                   elect.sync-chosen lane issues its tcgen05.mma groups:
 //                     S_t = Q_t K_jᵀ          (SS form, fp32 accumulator in TMEM)
 //                     O_t += P_t V_j          (TS form, P read from TMEM)
 //                   Two issuers keep the two tiles' chains independent: a
-//                   thread blocked on a full tensor-core queue while issuing
+//                   warp blocked on a full tensor-core queue while issuing
 //                   one tile's MMAs cannot delay the other tile.  For
 //                   d_qk == d_v they take turns per issue group (tile 0 group
 //                   g, tile 1 group g, tile 0 group g+1, ...) so the tensor
@@ -22,8 +23,10 @@
 //                   sm_103 reducing TMEM load (values + per-32-column max),
 //                   masks only boundary tiles (software 3-input max there),
 //                   exp2, lazy O rescale (threshold kRescaleLog2), writes P_t
-//                   as bf16 into the S_t columns, and at the end normalises
-//                   O_t and stores O and the LSE.
+//                   as bf16 into the S_t columns (in two halves for small
+//                   d_v, VarlenCfg::split_pv), and at the end normalises O_t
+//                   and writes O (through the dead Q tile and bulk copies
+//                   where VarlenCfg::stage_o) and the LSE.
 //
 // TMEM (512 columns x 128 lanes x 32 bit):
 //   [  0,128) S_0 / P_0   [128,256) S_1 / P_1   [256,384) O_0   [384,512) O_1
