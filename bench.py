@@ -338,8 +338,8 @@ def decode_launches_per_step(d, sm_count):
 def extra_lines(steps, warmup, device, peaks):
     """Secondary workloads (not the headline): device time, TFLOPS, roofline."""
     res = {}
-    for name in ["vit_window_d80", "vit_full_d128", "long_16384", "mla_causal", "mla_chunked",
-                 "mla_swa"]:
+    for name in ["vit_window_d80", "vit_window64_d80", "vit_full_d128", "long_16384",
+                 "mla_causal", "mla_chunked", "mla_swa"]:
         w = workloads.VARLEN_BENCH[name]()
         try:
             t, _, _, _, _ = time_varlen(w, steps, warmup, device, 1)

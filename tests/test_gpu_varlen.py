@@ -182,6 +182,26 @@ def test_strided_views(cuda_device, dqk, dv, H, Hk):
     assert torch.equal(out.cpu(), out2.cpu()) and torch.equal(lse.cpu(), lse2.cpu())
 
 
+def test_short_segments_packed(cuda_device):
+    # Runs of short segments (<= 64 rows, same token offsets in q and k) share
+    # work units under a block-diagonal mask; the mix also has a long segment
+    # between two runs and a zero-length one inside a run.
+    lens = [64] * 9 + [5, 1, 0, 33, 64, 17] + [700] + [40] * 7 + [63, 64, 2]
+    q, k, v, cq, ck = make(lens, lens, 4, 2, 80, 80, seed=18)
+    compare(q, k, v, cq, ck, 80 ** -0.5)
+    compare(q, k, v, cq, ck, 80 ** -0.5, causal=True)
+    compare(q, k, v, cq, ck, 80 ** -0.5, wl=16, wr=8)
+
+
+def test_short_segments_not_packed_when_k_differs(cuda_device):
+    # Short q segments against longer k segments (chunked prefill) are not
+    # packed: their rows see keys past their own q rows.
+    lq, lk = [30, 50, 20], [100, 50, 64]
+    q, k, v, cq, ck = make(lq, lk, 4, 4, 64, 64, seed=19)
+    compare(q, k, v, cq, ck, 0.125, causal=True)
+    compare(q, k, v, cq, ck, 0.125)
+
+
 def test_bitwise_deterministic(cuda_device):
     w = workloads.tiny()
     lens = [3000, 50, 1200]

@@ -329,7 +329,23 @@ __device__ __forceinline__ int snake_item(int round) {
 
 struct WorkItem {
   int q_start, k_start, lq, lk, head, kv_head, row0, n_qt, tile_lo, n_kv;
+  int b0, nb;  // first sequence of the unit and how many (nb > 1: a pack)
 };
+
+// Short segments: consecutive sequences of 1..kPackMaxLen query rows with as
+// many keys and the same token offsets in Q and K (self-attention over one
+// packed tensor, as in windowed ViT attention), whose first tokens fall in
+// the same kPackBlock-token block, form one work unit, a pack of at most
+// kPackBlock + kPackMaxLen rows.  Its query tiles run against its own key
+// tiles under a block-diagonal mask: each row sees only its own segment
+// (and the window inside it).  A 64-token window alone fills a quarter of a
+// 128 x 128 score tile; packed, up to four share two query tiles and two
+// key tiles.
+constexpr int kPackMaxLen = 64;
+constexpr int kPackBlock = kRowsPerItem - kPackMaxLen;  // 192
+// A unit in the sorted list: first sequence | number of sequences << 16.
+constexpr int kUnitShift = 16;
+static_assert(kMaxBatch < (1 << kUnitShift), "unit encoding");
 
 // ------------------------------------------------------------ bounded waits
 // Wait time limit for any pipeline barrier.  Normal waits are microseconds;
@@ -383,33 +399,70 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
 // Builds, in shared memory, the sequences sorted by key length (longest
 // first, ties by index) and the prefix sum of their work-item counts.
 // The key array doubles as the prefix array once the ranks are known.
-__device__ __forceinline__ void build_work_list(const VarlenArgs& a, int* s_prefix,
-                                                int* s_sorted, int* s_part) {
+// Builds the sorted unit list and the item prefix sums in shared memory.
+// s_tmp: 3 * kMaxBatch ints of scratch (the K ring, empty until the producer
+// starts), so that nothing is held in registers across the barriers.  Kept
+// out of line: it runs once per CTA, and inlined it changed the register
+// allocation of the pipeline loops (ViT d80 1.5 % slower).
+static __device__ __noinline__ void build_work_list(const VarlenArgs& a, int* s_prefix,
+                                                    int* s_sorted, int* s_part, int* s_tmp) {
   const int tid = threadIdx.x;
   const int B = a.batch;
-  int* s_key = s_prefix;
-  for (int b = tid; b < B; b += kVarlenThreads) s_key[b] = a.cu_k[b + 1] - a.cu_k[b];
-  __syncthreads();
+  int* t_lq = s_tmp;                 // query rows of sequence b
+  int* t_key = s_tmp + kMaxBatch;    // sort key of the unit starting at b, -1 for members
+  int* t_unit = s_tmp + 2 * kMaxBatch;  // nb of the unit starting at b (0 for members)
+  // 1. The only global reads: s_prefix[b] = the kPackBlock-token block of a
+  //    packable sequence's first token (-1 for any other sequence),
+  //    s_sorted[b] = its key count.
   for (int b = tid; b < B; b += kVarlenThreads) {
-    const int kb = s_key[b];
-    int rank = 0;
-    for (int o = 0; o < B; ++o) {
-      const int ko = s_key[o];
-      rank += (ko > kb) || (ko == kb && o < b);
-    }
-    s_sorted[rank] = b;
+    const int q0 = a.cu_q[b], k0 = a.cu_k[b];
+    const int lq = a.cu_q[b + 1] - q0, lk = a.cu_k[b + 1] - k0;
+    const bool pack = lq >= 1 && lq <= kPackMaxLen && lk == lq && k0 == q0;
+    s_prefix[b] = pack ? q0 / kPackBlock : -1;
+    s_sorted[b] = lk;
+    t_lq[b] = lq;
   }
   __syncthreads();
-  // Block-wide exclusive scan of per-sequence item counts in sorted order.
+  // 2. Units: a sequence starts one unless it continues its predecessor's
+  //    pack.  Sort key = key rows; the item count (heads x pairs of query
+  //    tiles) goes where the sequence's key count was.
+  for (int b = tid; b < B; b += kVarlenThreads) {
+    const int blk = s_prefix[b];
+    int nb = 0, key = -1;
+    if (!(blk >= 0 && b > 0 && s_prefix[b - 1] == blk)) {
+      nb = 1;
+      key = s_sorted[b];
+      if (blk >= 0)  // a pack: its members have as many query rows as keys
+        for (; b + nb < B && s_prefix[b + nb] == blk; ++nb) key += s_sorted[b + nb];
+      const int rows_q = blk >= 0 ? key : t_lq[b];
+      t_lq[b] = a.num_heads * ((max(rows_q, 0) + kRowsPerItem - 1) / kRowsPerItem);
+    } else {
+      t_lq[b] = 0;
+    }
+    t_key[b] = key;
+    t_unit[b] = nb;
+  }
+  __syncthreads();
+  // 3. Longest first: the rank of every entry by key (members last, ties in
+  //    sequence order); s_sorted[rank] = b | nb << kUnitShift and
+  //    s_prefix[rank] = its item count.
+  for (int b = tid; b < B; b += kVarlenThreads) {
+    const int kb = t_key[b];
+    int rank = 0;
+    for (int o = 0; o < B; ++o) {
+      const int ko = t_key[o];
+      rank += (ko > kb) || (ko == kb && o < b);
+    }
+    s_sorted[rank] = b | (t_unit[b] << kUnitShift);
+    s_prefix[rank] = t_lq[b];
+  }
+  __syncthreads();
+  // Block-wide exclusive scan of per-unit item counts in sorted order.
   const int per = (B + kVarlenThreads - 1) / kVarlenThreads;
   const int beg = tid * per;
   const int end = min(B, beg + per);
   int local = 0;
-  for (int p = beg; p < end; ++p) {
-    const int b = s_sorted[p];
-    const int lq = a.cu_q[b + 1] - a.cu_q[b];
-    local += a.num_heads * ((max(lq, 0) + kRowsPerItem - 1) / kRowsPerItem);
-  }
+  for (int p = beg; p < end; ++p) local += s_prefix[p];
   s_part[tid] = local;
   __syncthreads();
   if (tid < 32) {
@@ -440,12 +493,13 @@ __device__ __forceinline__ void build_work_list(const VarlenArgs& a, int* s_pref
   __syncthreads();
   int run = s_part[tid];
   for (int p = beg; p < end; ++p) {
+    const int n = s_prefix[p];  // item count in, exclusive prefix out
     s_prefix[p] = run;
-    const int b = s_sorted[p];
-    const int lq = a.cu_q[b + 1] - a.cu_q[b];
-    run += a.num_heads * ((max(lq, 0) + kRowsPerItem - 1) / kRowsPerItem);
+    run += n;
   }
   if (end == B && beg < end) s_prefix[B] = run;  // the thread owning the last chunk
+  // The scratch in s_tmp is overwritten next by TMA (async proxy).
+  ptx::fence_proxy_async_smem();
   __syncthreads();
 }
 
@@ -457,13 +511,15 @@ __device__ __forceinline__ WorkItem decode_item(int it, const VarlenArgs& a,
     const int mid = (lo + hi + 1) >> 1;
     if (s_prefix[mid] <= it) lo = mid; else hi = mid - 1;
   }
-  const int b = s_sorted[lo];
+  const int unit = s_sorted[lo];
   const int r = it - s_prefix[lo];
   WorkItem w;
-  w.q_start = a.cu_q[b];
-  w.k_start = a.cu_k[b];
-  w.lq = a.cu_q[b + 1] - w.q_start;
-  w.lk = a.cu_k[b + 1] - w.k_start;
+  w.b0 = unit & ((1 << kUnitShift) - 1);
+  w.nb = unit >> kUnitShift;
+  w.q_start = a.cu_q[w.b0];
+  w.k_start = a.cu_k[w.b0];
+  w.lq = a.cu_q[w.b0 + w.nb] - w.q_start;
+  w.lk = a.cu_k[w.b0 + w.nb] - w.k_start;
   const int pairs = (w.lq + kRowsPerItem - 1) / kRowsPerItem;
   w.head = r / pairs;
   const int pair = pairs - 1 - (r - w.head * pairs);  // later rows first
@@ -549,7 +605,10 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     ptx::tmem_alloc(ptx::smem_u32(&cb->tmem_base), 512);
     ptx::tmem_relinquish();
   }
-  build_work_list(args, s_prefix, s_sorted, s_part);  // ends with __syncthreads
+  static_assert(NK * C::k_slot_bytes >= 3 * kMaxBatch * (int)sizeof(int),
+                "the K ring holds the work-list scratch");
+  build_work_list(args, s_prefix, s_sorted, s_part,
+                  reinterpret_cast<int*>(k_ring));  // ends with __syncthreads
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -851,7 +910,20 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
       const bool row_valid = i < w.lq;
       const int off = w.lk - w.lq;
       int lo_i = 0, hi_i = 0;
-      if (row_valid) {
+      if (row_valid && w.nb > 1) {
+        // A pack of short segments: the row's own segment [s0, s1) (keys and
+        // rows share token offsets there), then the window inside it.
+        const int g = w.q_start + i;
+        int lo = w.b0, hi = w.b0 + w.nb - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (args.cu_q[mid] <= g) lo = mid; else hi = mid - 1;
+        }
+        const int s0 = args.cu_q[lo] - w.q_start, s1 = args.cu_q[lo + 1] - w.q_start;
+        lo_i = args.wl >= 0 ? max(s0, i - args.wl) : s0;
+        hi_i = args.wr >= 0 ? min(s1, i + args.wr + 1) : s1;
+        if (hi_i < lo_i) hi_i = lo_i;
+      } else if (row_valid) {
         lo_i = args.wl >= 0 ? max(0, i + off - args.wl) : 0;
         hi_i = args.wr >= 0 ? min(w.lk, i + off + args.wr + 1) : w.lk;
         if (hi_i < lo_i) hi_i = lo_i;

@@ -120,6 +120,15 @@ def vit_window(d: int = 80) -> VarlenWorkload:
                           d ** -0.5, qk_std=0.5, seed=1, return_lse=False)
 
 
+def vit_window64(d: int = 80) -> VarlenWorkload:
+    """The same tensors in 64-token windows (the Qwen2.5-VL windowed layers of
+    the sglang FA4 PR, "Speed Tests and Profiling": windows of 64 patches,
+    16 heads, d=80): 273 segments, the short-segment path."""
+    lens = window_lengths(VIT_LENGTHS, 64)
+    return VarlenWorkload(f"vit_window64_d{d}", lens, list(lens), 16, 16, d, d,
+                          d ** -0.5, qk_std=0.5, seed=1, return_lse=False)
+
+
 def long_seq(L: int) -> VarlenWorkload:
     return VarlenWorkload(f"long_{L}", [L], [L], 16, 16, 128, 128, 128 ** -0.5,
                           seed=2)
@@ -200,6 +209,7 @@ VARLEN_BENCH = {
     "vit_full_d72": lambda: vit_full(72),
     "vit_full_d128": lambda: vit_full(128),
     "vit_window_d80": lambda: vit_window(80),
+    "vit_window64_d80": lambda: vit_window64(80),
     "long_16384": lambda: long_seq(16384),
     "long_36864": lambda: long_seq(36864),
     "long_65536": lambda: long_seq(65536),
