@@ -404,10 +404,12 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
 // starts), so that nothing is held in registers across the barriers.  Kept
 // out of line: it runs once per CTA, and inlined it changed the register
 // allocation of the pipeline loops (ViT d80 1.5 % slower).
-static __device__ __noinline__ void build_work_list(const VarlenArgs& a, int* s_prefix,
-                                                    int* s_sorted, int* s_part, int* s_tmp) {
+// (The kernel arguments it needs come by value: a reference would make the
+// compiler copy the whole argument block to local memory for the call.)
+static __device__ __noinline__ void build_work_list(const int* cu_q, const int* cu_k, int B,
+                                                    int num_heads, int* s_prefix, int* s_sorted,
+                                                    int* s_part, int* s_tmp) {
   const int tid = threadIdx.x;
-  const int B = a.batch;
   int* t_lq = s_tmp;                 // query rows of sequence b
   int* t_key = s_tmp + kMaxBatch;    // sort key of the unit starting at b, -1 for members
   int* t_unit = s_tmp + 2 * kMaxBatch;  // nb of the unit starting at b (0 for members)
@@ -415,8 +417,8 @@ static __device__ __noinline__ void build_work_list(const VarlenArgs& a, int* s_
   //    packable sequence's first token (-1 for any other sequence),
   //    s_sorted[b] = its key count.
   for (int b = tid; b < B; b += kVarlenThreads) {
-    const int q0 = a.cu_q[b], k0 = a.cu_k[b];
-    const int lq = a.cu_q[b + 1] - q0, lk = a.cu_k[b + 1] - k0;
+    const int q0 = cu_q[b], k0 = cu_k[b];
+    const int lq = cu_q[b + 1] - q0, lk = cu_k[b + 1] - k0;
     const bool pack = lq >= 1 && lq <= kPackMaxLen && lk == lq && k0 == q0;
     s_prefix[b] = pack ? q0 / kPackBlock : -1;
     s_sorted[b] = lk;
@@ -435,7 +437,7 @@ static __device__ __noinline__ void build_work_list(const VarlenArgs& a, int* s_
       if (blk >= 0)  // a pack: its members have as many query rows as keys
         for (; b + nb < B && s_prefix[b + nb] == blk; ++nb) key += s_sorted[b + nb];
       const int rows_q = blk >= 0 ? key : t_lq[b];
-      t_lq[b] = a.num_heads * ((max(rows_q, 0) + kRowsPerItem - 1) / kRowsPerItem);
+      t_lq[b] = num_heads * ((max(rows_q, 0) + kRowsPerItem - 1) / kRowsPerItem);
     } else {
       t_lq[b] = 0;
     }
@@ -607,7 +609,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
   }
   static_assert(NK * C::k_slot_bytes >= 3 * kMaxBatch * (int)sizeof(int),
                 "the K ring holds the work-list scratch");
-  build_work_list(args, s_prefix, s_sorted, s_part,
+  build_work_list(args.cu_q, args.cu_k, args.batch, args.num_heads, s_prefix, s_sorted, s_part,
                   reinterpret_cast<int*>(k_ring));  // ends with __syncthreads
   ptx::tc_fence_before();
   __syncthreads();
