@@ -1,13 +1,18 @@
 """Benchmark: varlen attention forward TFLOPS and fraction of the GB300 roofline.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                        [--workload NAME] [--extra] [--no-cpu-baseline]
+                        [--workload NAME] [--no-extra] [--no-cpu-baseline]
 
 One step = one fa_varlen_fwd call over the whole packed batch of the
-workload (default: ViT encoder attention, packed images [576, 1024, 2304,
-4096, 256, 9216], 16 heads, head dim 80, non-causal).  Inputs are resident in
-HBM before timing; L2 is flushed (a 512 MB write) before every timed step and
-outside its CUDA-event pair.  Prints one JSON line on rank 0.
+workload.  The default workload is the largest single-GPU configuration: one
+65536-token image, 16 heads, head dim 128, non-causal, returning the LSE
+(`long_65536`).  Inputs are resident in HBM before timing; L2 is flushed (a
+512 MB write) before every timed step and outside its CUDA-event pair.
+Prints one JSON line on rank 0.  Unless --no-extra is given, the line also
+carries an "extra" block that times every other workload of the suite (ViT
+full and windowed at every head dim, the long sequences, the MLA prefill
+cases, sparse-MLA decode, split-KV and packed-GQA cases) with its roofline
+fraction; those inputs are drawn on the device (parity is the tests' job).
 
 `--impl reference` times the fp64 CPU oracle (the only reference arm this
 method has) on a bounded sample of the same workload and prints the same
@@ -165,11 +170,17 @@ def whole_job_rate(units_per_rank: float, ms_max: float, world: int) -> float:
 
 
 # ------------------------------------------------------------ CPU oracle timing
+_HOST_INPUTS = {}
+
+
 def oracle_sample_rate(w, budget_s: float, seed: int = 0):
     """Times the fp64 oracle on a random sample of (token, head) rows of the
     workload; returns (flops/s, rows, seconds, threads)."""
     import oracle
-    q, k, v, cq, ck = w.make_inputs()
+    if w.name not in _HOST_INPUTS:   # drawn once per workload, reused by every step
+        _HOST_INPUTS.clear()
+        _HOST_INPUTS[w.name] = w.make_inputs()
+    q, k, v, cq, ck = _HOST_INPUTS[w.name]
     rng = np.random.default_rng(seed)
     counts = np.concatenate([metrics.visible_keys_per_row(lq, lk, w.causal, *w.window)
                              for lq, lk in zip(w.lens_q, w.lens_k)])
@@ -183,17 +194,24 @@ def oracle_sample_rate(w, budget_s: float, seed: int = 0):
         flops = 2.0 * float(counts[rows // w.num_heads].sum()) * (w.d_qk + w.d_v)
         return flops, dt, n
 
-    flops, dt, n = run(256)
-    target = max(256, min(n_rows_total, int(n * budget_s / max(dt, 1e-3))))
+    flops, dt, n = run(32)
+    target = max(32, min(n_rows_total, int(n * budget_s / max(dt, 1e-3))))
     flops, dt, n = run(target)
     return flops / dt, n, dt, oracle.num_threads()
 
 
 # ------------------------------------------------------------ GPU timing
-def time_varlen(w, steps, warmup, device, world):
+def time_varlen(w, steps, warmup, device, world, on_device=False, e2e=True):
+    """CUDA-event times of fa_varlen_fwd on workload w (L2 flushed before each
+    step, outside the events), the clocks seen meanwhile, and (e2e) the end
+    to end time per step with pinned host inputs copied in and the outputs
+    copied back."""
     import varlen_flashattention_forward_gb300 as fa
-    q, k, v, cq, ck = w.make_inputs()
-    qd, kd, vd, cqd, ckd = (t.to(device) for t in (q, k, v, cq, ck))
+    if on_device:
+        qd, kd, vd, cqd, ckd = w.make_inputs_on(device)
+    else:
+        q, k, v, cq, ck = w.make_inputs()
+        qd, kd, vd, cqd, ckd = (t.to(device) for t in (q, k, v, cq, ck))
     out = torch.empty((w.total_q, w.num_heads, w.d_v), dtype=torch.bfloat16, device=device)
     lse = (torch.empty((w.num_heads, w.total_q), dtype=torch.float32, device=device)
            if w.return_lse else None)
@@ -220,13 +238,20 @@ def time_varlen(w, steps, warmup, device, world):
         torch.cuda.synchronize(device)
     barrier(world)
     times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if not e2e:
+        if fa.fa_get_device_status() != fa.FA_OK:
+            raise RuntimeError("device status word set during timing")
+        return times_ms, clk.summary(), None, 0, 0
 
     # End to end through the public API with host buffers: pinned host inputs
-    # copied in, kernel, output copied back, every step.
+    # copied in, kernel, outputs (O and, if returned, the LSE) copied back,
+    # every step.
     hq, hk, hv, hcq, hck = (t.pin_memory() for t in (q, k, v, cq, ck))
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory() if lse is not None else None
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hcq, hck))
-    d2h = hout.numel() * hout.element_size()
+    d2h = hout.numel() * hout.element_size() + (
+        hlse.numel() * hlse.element_size() if hlse is not None else 0)
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     e2e_steps = max(3, min(steps, 10))
@@ -242,6 +267,8 @@ def time_varlen(w, steps, warmup, device, world):
         ckd.copy_(hck, non_blocking=True)
         fa.fa_varlen_fwd(*args)
         hout.copy_(out, non_blocking=True)
+        if hlse is not None:
+            hlse.copy_(lse, non_blocking=True)
     e_end.record(stream)
     torch.cuda.synchronize(device)
     e2e_ms = e_start.elapsed_time(e_end) / e2e_steps
@@ -250,7 +277,7 @@ def time_varlen(w, steps, warmup, device, world):
     return times_ms, clk.summary(), e2e_ms, h2d, d2h
 
 
-def time_decode(d, steps, warmup, device, world):
+def time_decode(d, steps, warmup, device, world, e2e=True):
     """Device time of fa_sparse_mla_decode on the decode workload (inputs drawn
     on the device for speed; parity is covered by the tests), and the end to
     end time with the step's inputs (Q, page table, top-k indices) copied in
@@ -281,6 +308,11 @@ def time_decode(d, steps, warmup, device, world):
     torch.cuda.synchronize(device)
     barrier(world)
     ts = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if not e2e:
+        if fa.fa_get_device_status() != fa.FA_OK:
+            raise RuntimeError("device status word set during timing")
+        del cache
+        return ts, None, 0, 0
 
     hq, hpt, hti = q.cpu().pin_memory(), pt.cpu().pin_memory(), ti.cpu().pin_memory()
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -317,52 +349,62 @@ def time_decode(d, steps, warmup, device, world):
     return ts, e2e_ms, h2d, d2h
 
 
-def decode_launches_per_step(d, sm_count):
-    """Kernel launches of one fa_sparse_mla_decode call: 1, or 2 when the host
-    picks the equal-tile split (whose cut units are merged by a second
-    kernel).  Mirrors the schedule choice in csrc/fa_api.cu (plan_decode)."""
-    groups = (d.num_heads + 63) // 64
-    n_tiles = d.topk // 64
-    units = d.num_tokens * groups
-    total = units * n_tiles
-    cdiv = lambda x, y: -(-x // y)
-    upc = 32 // n_tiles
-    grid_u = max(cdiv(units, upc), min(units, sm_count))
-    cost_u = cdiv(grid_u, sm_count) * cdiv(units, grid_u) * n_tiles
-    grid_t = min(cdiv(total, 32 * sm_count) * sm_count, max(1, total // 2))
-    cuts = units % grid_t != 0
-    cost_t = cdiv(grid_t, sm_count) * cdiv(total, grid_t) + (6 if cuts else 0)
-    return 2 if (cuts and cost_t < cost_u and grid_t >= 2) else 1
+def decode_launches_per_step(d):
+    """Kernel launches of one fa_sparse_mla_decode call of this size, as the
+    library's own planner (fa_sparse_mla_decode_plan) gives them: 1, or 2
+    when the split cuts tokens between CTAs and a merge kernel combines them."""
+    import varlen_flashattention_forward_gb300 as fa
+    launches, _ = fa.fa_sparse_mla_decode_plan(d.num_tokens, d.num_heads, d.topk)
+    return launches
 
 
-def extra_lines(steps, warmup, device, peaks):
-    """Secondary workloads (not the headline): device time, TFLOPS, roofline."""
+def _roofline(flops, byts, ms, peaks):
+    """Bound, and the fraction of the roofline time (the slower of compute at
+    the bf16 peak and bytes at the HBM copy rate) the measured time reaches."""
+    t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
+    return ("tensor" if t_tensor >= t_hbm else "hbm"), max(t_tensor, t_hbm) * 1e3 / ms
+
+
+EXTRA_VARLEN = ["tiny", "vit_full_d64", "vit_full_d72", "vit_full_d80", "vit_full_d128",
+                "vit_window_d64", "vit_window_d72", "vit_window_d80", "vit_window_d128",
+                "vit_window64_d80", "long_16384", "long_36864", "long_65536", "mla_causal",
+                "mla_chunked", "mla_swa"]
+
+
+def extra_lines(steps, warmup, device, peaks, skip=()):
+    """Every other workload of the suite: device time (mean and best of the
+    steps), TFLOPS, GB/s and the roofline fraction."""
     res = {}
-    for name in ["vit_window_d80", "vit_window64_d80", "vit_full_d128", "long_16384",
-                 "mla_causal", "mla_chunked", "mla_swa"]:
-        w = workloads.VARLEN_BENCH[name]()
+    for name in EXTRA_VARLEN + [n for n in workloads.EXTRA_ONLY if n not in EXTRA_VARLEN]:
+        if name in skip:
+            continue
+        w = (workloads.VARLEN_BENCH.get(name) or workloads.EXTRA_ONLY[name])()
         try:
-            t, _, _, _, _ = time_varlen(w, steps, warmup, device, 1)
+            t, _, _, _, _ = time_varlen(w, steps, warmup, device, 1, on_device=True, e2e=False)
         except Exception as exc:  # report and continue with the rest
             res[name] = {"error": str(exc)[:200]}
             continue
         ms = statistics.mean(t)
         flops = metrics.varlen_flops(w)
         byts = metrics.varlen_alg_bytes(w)
-        t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
-        res[name] = {"ms": round(ms, 4), "tflops": round(flops / ms / 1e9, 1),
-                     "gbs": round(byts / ms / 1e6, 1),
-                     "roofline_frac": round(t_roof * 1e3 / ms, 4)}
+        bound, frac = _roofline(flops, byts, ms, peaks)
+        res[name] = {"ms": round(ms, 4), "ms_min": round(min(t), 4),
+                     "tflops": round(flops / ms / 1e9, 1), "gbs": round(byts / ms / 1e6, 1),
+                     "bound": bound, "roofline_frac": round(frac, 4)}
+        torch.cuda.empty_cache()
     try:
         d = workloads.DecodeWorkload()
-        t, _, _, _ = time_decode(d, steps, warmup, device, 1)
+        t, _, _, _ = time_decode(d, steps, warmup, device, 1, e2e=False)
         ms = statistics.mean(t)
         byts = metrics.decode_alg_bytes(d)
-        res["decode"] = {"ms": round(ms, 4), "gbs": round(byts / ms / 1e6, 1),
+        res["decode"] = {"ms": round(ms, 4), "ms_min": round(min(t), 4),
+                         "gbs": round(byts / ms / 1e6, 1), "bound": "hbm",
                          "hbm_frac": round(byts / ms / 1e6 / peaks["hbm_gbs"], 4),
                          "tflops": round(metrics.decode_flops(d) / ms / 1e9, 1)}
     except Exception as exc:
         res["decode"] = {"error": str(exc)[:200]}
+    torch.cuda.empty_cache()
     return res
 
 
@@ -431,7 +473,6 @@ def main_decode(a, world, rank, local, peaks):
     e2e_ms = max_over_ranks(e2e_ms, world)
     if rank != 0:
         return
-    sms = torch.cuda.get_device_properties(device).multi_processor_count
     gbs = byts / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(whole_job_rate(byts, ms, world) / 1e9, 1), "unit": "GB/s",
@@ -449,7 +490,7 @@ def main_decode(a, world, rank, local, peaks):
         "tflops": round(metrics.decode_flops(d) / (ms * 1e-3) / 1e12, 1),
         "e2e": {"value": round(whole_job_rate(byts, e2e_ms, world) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": a.steps * decode_launches_per_step(d, sms), "clocks": clk.summary(),
+        "gpu_launches": a.steps * decode_launches_per_step(d), "clocks": clk.summary(),
     }
     if not a.no_cpu_baseline:
         rate, n, dt, threads = decode_oracle_rate(d, a.cpu_budget)
@@ -464,9 +505,10 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="vit_full_d80",
+    ap.add_argument("--workload", default="long_65536",
                     help="a varlen workload name or 'decode'")
-    ap.add_argument("--extra", action="store_true", help="also time the other workloads")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time the headline workload only (no extra block)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-tokens", type=int, default=0,
                     help="decode workload with this many tokens (default: 128)")
@@ -547,8 +589,12 @@ def main():
         line["cpu_baseline"] = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": threads,
                                 "kind": "oracle",
                                 "sample": f"{n} random (token, head) rows, {dt:.1f} s, fp64"}
-    if a.extra:
-        line["extra"] = extra_lines(max(3, a.steps // 4), 3, device, peaks)
+    if not a.no_extra and world == 1:
+        line["extra"] = extra_lines(max(5, a.steps // 2), 3, device, peaks, skip=(w.name,))
+        line["extra_note"] = ("every other workload, inputs drawn on the device, "
+                              f"{max(5, a.steps // 2)} timed steps each after 3 warm-up steps, "
+                              "L2 flushed before each step; roofline_frac = max(flops / bf16 "
+                              "burst peak, alg. bytes / HBM copy peak) / time")
     print(json.dumps(line))
 
 

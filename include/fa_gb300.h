@@ -15,8 +15,12 @@
  *     q/k/v views fa_varlen_fwd_strided takes), 16-byte aligned.  bf16 means
  *     IEEE bfloat16 bit patterns (2 bytes).
  *   - Calls are asynchronous on `stream` (NULL = legacy default stream).  The
- *     library allocates no memory, performs no host<->device copy and never
- *     synchronises; it only encodes TMA descriptors on the host and launches.
+ *     library performs no host<->device copy and never synchronises; it only
+ *     encodes TMA descriptors on the host and launches.  It allocates no
+ *     device memory per call.  The one exception is a one-time allocation:
+ *     fa_sparse_mla_decode allocates a partial-result workspace for a
+ *     (device, stream) on the first call there that needs one (see that
+ *     entry point).  fa_sparse_mla_decode_noalloc never allocates.
  *     The first call on a device queries device attributes once; make it
  *     before any stream capture that is to contain a call.
  *   - Errors detected on the host (argument checks) are returned before any
@@ -50,6 +54,8 @@
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
+
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -157,12 +163,22 @@ fa_status fa_varlen_fwd_strided(const void* q, long long q_row_stride, long long
  *   out           bf16 [num_tokens, num_heads, 512]: sum_j p_j * row_j[0:512]
  *   lse           fp32 [num_heads, num_tokens] or NULL
  *
- * The (token, head group, 64-key tile) work is spread evenly over the SMs;
- * when a token's keys end up on several CTAs, their partial results go to a
- * workspace allocated stream-ordered on `stream` (from a pool the library
- * keeps for the device) and a second kernel merges them by their
- * log-sum-exp [flash_attn] (FA4SplitKVCombineKernel).  Both launches and the workspace's
- * allocation and release are ordered on `stream`.
+ * The (token, head group, 64-key tile) work is spread evenly over the SMs.
+ * When a token's keys end up on several CTAs, their partial results go to a
+ * workspace, and a second kernel on `stream` merges them by their
+ * log-sum-exp [flash_attn] (FA4SplitKVCombineKernel).
+ *
+ * Workspace ownership: the library keeps one workspace per (device, stream)
+ * for the life of the process.  The first call on a stream whose split needs
+ * one allocates it with cudaMalloc; later calls reuse it and allocate
+ * nothing.  A call that needs more than the stream's workspace holds
+ * allocates a larger one and keeps the old one allocated, so a CUDA graph
+ * captured earlier stays valid.  fa_sparse_mla_decode_plan gives the size a
+ * call needs.  Make the first call on a stream before any stream capture
+ * that is to contain a call.  Calls on one stream share its workspace in
+ * stream order.  Per-thread default streams of different host threads share
+ * one workspace per device, so they must not run decode calls at the same
+ * time.  At most two waves of CTAs split (about 80 MB on 152 SMs).
  *
  * Host errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (heads, topk),
  * FA_ERR_ARCH, FA_ERR_LAUNCH (launch or workspace allocation failed).
@@ -173,6 +189,23 @@ fa_status fa_sparse_mla_decode(const void* q, const void* kv_cache,
                                int num_pages, int max_pages_per_tok,
                                float softmax_scale, void* out, float* lse,
                                fa_stream_t stream);
+
+/*
+ * fa_sparse_mla_decode_plan -- the work split fa_sparse_mla_decode (and
+ * fa_sparse_mla_decode_noalloc) would use for a call of this size on the
+ * current device, without launching anything.
+ *
+ *   *launches         kernel launches of the call: 0 (no tokens), 1, or 2
+ *                     (the split cuts tokens between CTAs and a merge
+ *                     kernel combines them)
+ *   *workspace_bytes  partial-result workspace the call needs (0 with one
+ *                     launch)
+ *
+ * Host errors: FA_ERR_INVALID_ARG (null outputs, negative sizes),
+ * FA_ERR_UNSUPPORTED (heads, topk as fa_sparse_mla_decode), FA_ERR_ARCH.
+ */
+fa_status fa_sparse_mla_decode_plan(int num_tokens, int num_heads, int topk, int* launches,
+                                    size_t* workspace_bytes);
 
 /*
  * fa_sparse_mla_decode_noalloc -- fa_sparse_mla_decode without any device
@@ -192,9 +225,17 @@ fa_status fa_sparse_mla_decode(const void* q, const void* kv_cache,
  *   - Calls that can overlap in time on one device (different streams, or
  *     different host threads) race on the shared scratch: the caller must
  *     order them.
- *   - The first call on each device does one-time setup (module load,
- *     scratch address lookup, kernel attributes); make that first call
+ *   - The first call on each device does one-time setup (scratch address
+ *     lookup, kernel attributes, and, under CUDA's lazy module loading, the
+ *     load of the module that holds the scratch); make that first call
  *     before any stream capture.
+ *   - The scratch's device address is looked up once per device and kept;
+ *     after a cudaDeviceReset it no longer holds, so no call may follow a
+ *     cudaDeviceReset in the same process.
+ *   - With lazy module loading (CUDA_MODULE_LOADING=LAZY, the default since
+ *     CUDA 12.2) the scratch is committed on a device only by the first call
+ *     there; with eager loading, every process that loads the library
+ *     commits it on every device it uses.
  *
  * Host errors: those of fa_sparse_mla_decode, and FA_ERR_SCRATCH.
  */

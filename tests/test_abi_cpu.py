@@ -150,3 +150,26 @@ def test_valid_arguments_without_gpu_fail_cleanly(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert varlen(lib) in (fa.FA_ERR_LAUNCH, fa.FA_ERR_ARCH)
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((4, 64, 256, True, True), None),            # valid: past the checks
+    ((4, 64, 256, False, True), fa.FA_ERR_INVALID_ARG),
+    ((4, 64, 256, True, False), fa.FA_ERR_INVALID_ARG),
+    ((-1, 64, 256, True, True), fa.FA_ERR_INVALID_ARG),
+    ((4, 48, 256, True, True), fa.FA_ERR_UNSUPPORTED),
+    ((4, 64, 200, True, True), fa.FA_ERR_UNSUPPORTED),
+    ((4, 64, 4096, True, True), fa.FA_ERR_UNSUPPORTED),
+])
+def test_decode_plan_host_validation(lib, args, expect):
+    import torch
+    T, H, topk, with_n, with_b = args
+    n, b = ctypes.c_int(-5), ctypes.c_size_t(7)
+    st = lib.fa_sparse_mla_decode_plan(T, H, topk, ctypes.byref(n) if with_n else None,
+                                       ctypes.byref(b) if with_b else None)
+    if expect is None:
+        if torch.cuda.is_available():
+            pytest.skip("a GPU is present")
+        assert st in (fa.FA_ERR_LAUNCH, fa.FA_ERR_ARCH)
+    else:
+        assert st == expect

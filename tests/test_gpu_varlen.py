@@ -232,8 +232,9 @@ def sample_rows(lens_q, H, n, seed):
     return np.unique(toks * H + heads)
 
 
-FULL = ["vit_full_d80", "vit_full_d64", "vit_full_d72", "vit_full_d128", "vit_window_d80",
-        "long_16384", "long_65536", "mla_causal", "mla_chunked", "mla_swa"]
+FULL = ["vit_full_d80", "vit_full_d64", "vit_full_d72", "vit_full_d128", "vit_window_d64",
+        "vit_window_d72", "vit_window_d80", "vit_window_d128", "long_16384", "long_36864",
+        "long_65536", "mla_causal", "mla_chunked", "mla_swa"]
 
 
 @pytest.mark.parametrize("name", FULL)

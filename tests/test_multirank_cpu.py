@@ -65,7 +65,8 @@ def test_whole_job_rate_single_rank():
     assert bench.whole_job_rate(5e12, 10.0, 4) == pytest.approx(2e15)
 
 
-@pytest.mark.parametrize("extra", [["--workload", "decode", "--decode-tokens", "2"], []],
+@pytest.mark.parametrize("extra", [["--workload", "decode", "--decode-tokens", "2"],
+                                   ["--workload", "vit_full_d80"]],
                          ids=["decode", "varlen"])
 def test_reference_arm_under_torchrun(extra):
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1", "--nproc-per-node",

@@ -45,22 +45,19 @@ def test_noalloc_matches_allocating_entry(cuda_device, T, H, topk, context):
 
 
 def test_noalloc_rejects_split_beyond_scratch(cuda_device):
-    """200 units of 32 tiles go to the split schedule over two waves of SMs;
-    its partial results need more than the fixed scratch: FA_ERR_SCRATCH,
-    and nothing is written."""
+    """A call whose split needs more partial-result space than the fixed
+    scratch holds returns FA_ERR_SCRATCH and writes nothing.  The planned
+    workspace comes from the library's own planner: 200 units of 32 tiles
+    go to the split over two waves of SMs on a GB300."""
     T, H, topk, pages = 200, 64, 2048, 32
+    launches, need = fa.fa_sparse_mla_decode_plan(T, H, topk)
+    if need <= fa.NOALLOC_SCRATCH_BYTES:
+        pytest.skip(f"this device's split needs {need} bytes, which fits the scratch")
     dev = torch.device("cuda:0")
     q = torch.zeros((T, H, 576), dtype=torch.bfloat16, device=dev)
     cache = torch.zeros((pages, 64, 576), dtype=torch.bfloat16, device=dev)
     pt = torch.arange(pages, dtype=torch.int32, device=dev).repeat(T, 1)
     ti = torch.arange(topk, dtype=torch.int32, device=dev).repeat(T, 1)
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    tiles = T * (topk // 64)
-    waves = -(-tiles // (32 * sms))
-    grid = waves * sms
-    need = 2 * grid * 64 * (512 + 1) * 4
-    if need <= fa.NOALLOC_SCRATCH_BYTES:
-        pytest.skip(f"{sms} SMs: this split fits the scratch")
     out = torch.full((T, H, 512), 7.0, dtype=torch.bfloat16, device=dev)
     with pytest.raises(fa.FaError) as e:
         fa.fa_sparse_mla_decode_noalloc(q, cache, pt, ti, 576 ** -0.5, out)

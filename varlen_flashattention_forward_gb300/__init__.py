@@ -13,6 +13,9 @@ Entry points (same names as the C ABI):
                 stream=None)
   fa_sparse_mla_decode(q, kv_cache, page_table, topk_idx, softmax_scale,
                        out=None, lse=None, return_lse=False, stream=None)
+  fa_sparse_mla_decode_plan(num_tokens, num_heads, topk)
+  fa_sparse_mla_decode_noalloc(q, kv_cache, page_table, topk_idx, softmax_scale,
+                               out, lse=None, stream=None)
   fa_merge_attn_states(prefix_out, prefix_lse, suffix_out, suffix_lse,
                        out=None, out_lse=None, stream=None)
   fa_get_device_status()
@@ -36,8 +39,8 @@ LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
 
 # Exported C symbols (kept in sync with include/fa_gb300.h; a CPU test checks).
 EXPORTS = ("fa_varlen_fwd", "fa_varlen_fwd_strided", "fa_sparse_mla_decode",
-           "fa_sparse_mla_decode_noalloc", "fa_merge_attn_states", "fa_get_device_status",
-           "fa_status_string")
+           "fa_sparse_mla_decode_plan", "fa_sparse_mla_decode_noalloc", "fa_merge_attn_states",
+           "fa_get_device_status", "fa_status_string")
 
 _lib = None
 
@@ -70,6 +73,9 @@ def load_library():
     lib.fa_sparse_mla_decode.argtypes = [p, p, p, p, i32, i32, i32, i32, i32,
                                          f32, p, p, p]
     lib.fa_sparse_mla_decode.restype = i32
+    lib.fa_sparse_mla_decode_plan.argtypes = [i32, i32, i32, ctypes.POINTER(i32),
+                                              ctypes.POINTER(ctypes.c_size_t)]
+    lib.fa_sparse_mla_decode_plan.restype = i32
     lib.fa_sparse_mla_decode_noalloc.argtypes = [p, p, p, p, i32, i32, i32, i32, i32,
                                                  f32, p, p, p]
     lib.fa_sparse_mla_decode_noalloc.restype = i32
@@ -208,6 +214,19 @@ def fa_sparse_mla_decode(q, kv_cache, page_table, topk_idx, softmax_scale=None,
     if st != FA_OK:
         raise FaError(st, "fa_sparse_mla_decode")
     return (out, lse) if lse is not None else out
+
+
+def fa_sparse_mla_decode_plan(num_tokens, num_heads, topk):
+    """(launches, workspace_bytes) of a decode call of this size on the
+    current device; see fa_sparse_mla_decode_plan in include/fa_gb300.h."""
+    lib = load_library()
+    n = ctypes.c_int(0)
+    b = ctypes.c_size_t(0)
+    st = lib.fa_sparse_mla_decode_plan(int(num_tokens), int(num_heads), int(topk),
+                                       ctypes.byref(n), ctypes.byref(b))
+    if st != FA_OK:
+        raise FaError(st, "fa_sparse_mla_decode_plan")
+    return n.value, b.value
 
 
 def fa_sparse_mla_decode_noalloc(q, kv_cache, page_table, topk_idx, softmax_scale, out,

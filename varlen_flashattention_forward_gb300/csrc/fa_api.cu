@@ -3,15 +3,19 @@
 // head-dim instantiations, and the device status word.
 //
 // No function here copies data or synchronises, except fa_get_device_status
-// (documented as synchronising).  The only device memory allocated is the
-// partial-result workspace of fa_sparse_mla_decode, stream-ordered from a
-// library-owned pool that keeps its memory between calls.
+// (documented as synchronising).  The only device memory the library
+// allocates is the partial-result workspace of fa_sparse_mla_decode: one
+// buffer per (device, stream), allocated by the first call on that stream
+// whose work split needs it and reused by every later call; a call that needs
+// more than the stream's buffer holds allocates a larger one and keeps the
+// old one allocated (a CUDA graph captured earlier may still point at it).
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -43,7 +47,6 @@ struct DeviceInfo {
   bool arch_ok = false;
   int sm_count = 0;
   unsigned int* status = nullptr;  // device address of g_fa_status
-  cudaMemPool_t pool = nullptr;    // decode workspace pool, created on first need
 };
 
 std::mutex g_mu;
@@ -116,29 +119,46 @@ bool encode_rows(CUtensorMap* m, const void* base, int dim, int heads, int token
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The device's workspace pool: memory freed back to it stays reserved
-// (release threshold = max), so steady-state calls do not reach the driver's
-// allocator.
-cudaMemPool_t workspace_pool(DeviceInfo* d) {
+// Decode workspace of one (device, stream).  Calls on one stream run in
+// order, so they can share it; calls on different streams get their own.
+struct StreamWorkspace {
+  int dev;
+  cudaStream_t stream;
+  void* ptr;
+  size_t bytes;
+};
+std::vector<StreamWorkspace> g_ws;    // guarded by g_mu
+std::vector<void*> g_ws_outgrown;     // replaced buffers, kept allocated
+
+// The workspace of `stream` on the current device, at least `need` bytes.
+// Allocates (cudaMalloc) only when the stream has none yet or a smaller one.
+fa_status stream_workspace(cudaStream_t stream, size_t need, void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_LAUNCH;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!d->pool) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-    cudaMemPoolProps props;
-    std::memset(&props, 0, sizeof props);
-    props.allocType = cudaMemAllocationTypePinned;
-    props.location.type = cudaMemLocationTypeDevice;
-    props.location.id = dev;
-    cudaMemPool_t pool = nullptr;
-    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
-    uint64_t keep = UINT64_MAX;
-    if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
-      cudaMemPoolDestroy(pool);
-      return nullptr;
-    }
-    d->pool = pool;
+  StreamWorkspace* w = nullptr;
+  for (auto& e : g_ws)
+    if (e.dev == dev && e.stream == stream) w = &e;
+  if (w && w->bytes >= need) {
+    *out = w->ptr;
+    return FA_OK;
   }
-  return d->pool;
+  // Round up to 4 MiB so that slowly growing requests reallocate rarely.
+  const size_t bytes = (need + (4u << 20) - 1) / (4u << 20) * (4u << 20);
+  void* p = nullptr;
+  if (cudaMalloc(&p, bytes) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free allocation error
+    return FA_ERR_LAUNCH;
+  }
+  if (w) {
+    g_ws_outgrown.push_back(w->ptr);
+    w->ptr = p;
+    w->bytes = bytes;
+  } else {
+    g_ws.push_back(StreamWorkspace{dev, stream, p, bytes});
+  }
+  *out = p;
+  return FA_OK;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -269,6 +289,44 @@ extern "C" fa_status fa_varlen_fwd_strided(
 
 namespace {
 
+// Work split of a decode call.  Each CTA takes a contiguous range of the
+// (token, head group) units' 64-key tiles, at most kDecodeMaxTilesPerCta of
+// them.  Either the ranges hold whole units, or they hold equal tile counts
+// over whole waves of SMs and the units cut by a range end are merged by a
+// second kernel.  The host takes the cut with the fewer tiles on the busiest
+// SM, counting the merge as kDecodeMergeCostTiles tiles; the equal-tile cut
+// is considered only up to two waves, which bounds its workspace.
+struct DecodeSplit {
+  long long grid;
+  int gran;     // tiles per granule: 1 (equal tiles) or n_tiles (whole units)
+  bool split;   // partial results and the merge kernel are needed
+};
+
+DecodeSplit decode_split(long long units, int n_tiles, long long sms) {
+  auto ceil_div = [](long long x, long long y) { return (x + y - 1) / y; };
+  const long long total = units * n_tiles;
+  // Whole units per CTA.
+  const long long upc = fa::kDecodeMaxTilesPerCta / n_tiles;
+  const long long grid_u = std::max(ceil_div(units, upc), std::min(units, sms));
+  const long long cost_u = ceil_div(grid_u, sms) * ceil_div(units, grid_u) * n_tiles;
+  // Equal tile counts, over whole waves of SMs, at least 2 tiles per CTA.
+  long long grid_t = ceil_div(total, fa::kDecodeMaxTilesPerCta * sms) * sms;
+  grid_t = std::min(grid_t, std::max(1LL, total / 2));
+  const bool cuts = units % grid_t != 0;
+  const long long cost_t = ceil_div(grid_t, sms) * ceil_div(total, grid_t) +
+                           (cuts ? fa::kDecodeMergeCostTiles : 0);
+  DecodeSplit d;
+  d.split = cuts && cost_t < cost_u && grid_t <= 2 * sms;
+  const bool equal = d.split || (!cuts && grid_t <= 2 * sms);
+  d.grid = equal ? grid_t : grid_u;
+  d.gran = equal ? 1 : n_tiles;
+  return d;
+}
+
+size_t decode_workspace_bytes(const DecodeSplit& d) {
+  return d.split ? (size_t)2 * d.grid * 64 * (fa::kDv + 1) * sizeof(float) : 0;
+}
+
 // Everything fa_sparse_mla_decode does before it needs workspace memory:
 // argument checks, the Q tensor map, the kernel arguments and the work split
 // (see the comment below).  `*launch` is false when there is nothing to run.
@@ -342,37 +400,19 @@ fa_status plan_decode(const void* q, const void* kv_cache, const int* page_table
   a.status = dev->status;
   a.groups = groups;
   a.n_tiles = n_tiles;
-  // Work split.  Each CTA takes a contiguous range of the (token, head group)
-  // units' 64-key tiles, at most kDecodeMaxTilesPerCta of them.  Either the
-  // ranges hold whole units, or they hold equal tile counts and the units cut
-  // by a range end are merged by a second kernel.  The host takes the cut
-  // with the fewer tiles on the busiest SM, counting the merge as
-  // kDecodeMergeCostTiles tiles.
-  const long long sms = dev->sm_count;
-  auto ceil_div = [](long long x, long long y) { return (x + y - 1) / y; };
-  // Whole units per CTA.
-  const long long upc = fa::kDecodeMaxTilesPerCta / n_tiles;
-  const long long grid_u = std::max(ceil_div(units, upc), std::min(units, sms));
-  const long long cost_u = ceil_div(grid_u, sms) * ceil_div(units, grid_u) * n_tiles;
-  // Equal tile counts, over whole waves of SMs, at least 2 tiles per CTA.
-  long long grid_t = ceil_div(total, fa::kDecodeMaxTilesPerCta * sms) * sms;
-  grid_t = std::min(grid_t, std::max(1LL, total / 2));
-  const bool cuts = units % grid_t != 0;
-  const long long cost_t = ceil_div(grid_t, sms) * ceil_div(total, grid_t) +
-                           (cuts ? fa::kDecodeMergeCostTiles : 0);
-  plan->split = cuts && cost_t < cost_u;
-  const long long grid = plan->split || !cuts ? grid_t : grid_u;
+  const DecodeSplit sp = decode_split(units, n_tiles, dev->sm_count);
+  plan->split = sp.split;
   a.total_tiles = (int)total;
-  a.grid = (int)grid;
-  a.gran = plan->split || !cuts ? 1 : n_tiles;
+  a.grid = (int)sp.grid;
+  a.gran = sp.gran;
   const long long granules = total / a.gran;
-  a.range_q = (int)(granules / grid);
-  a.range_r = (int)(granules % grid);
+  a.range_q = (int)(granules / sp.grid);
+  a.range_r = (int)(granules % sp.grid);
   a.part_o = nullptr;
   a.part_lse = nullptr;
   if (plan->split) {
-    plan->o_bytes = (size_t)2 * grid * 64 * fa::kDv * sizeof(float);
-    plan->l_bytes = (size_t)2 * grid * 64 * sizeof(float);
+    plan->o_bytes = (size_t)2 * sp.grid * 64 * fa::kDv * sizeof(float);
+    plan->l_bytes = (size_t)2 * sp.grid * 64 * sizeof(float);
   }
   return FA_OK;
 }
@@ -428,17 +468,33 @@ extern "C" fa_status fa_sparse_mla_decode(const void* q, const void* kv_cache,
   cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
   void* ws = nullptr;
   if (plan.split) {
-    DeviceInfo* dev = nullptr;
-    st = device_info(&dev);
+    st = stream_workspace(st_, plan.o_bytes + plan.l_bytes, &ws);
     if (st != FA_OK) return st;
-    cudaMemPool_t pool = workspace_pool(dev);
-    if (!pool) return FA_ERR_LAUNCH;
-    if (cudaMallocFromPoolAsync(&ws, plan.o_bytes + plan.l_bytes, pool, st_) != cudaSuccess)
-      return FA_ERR_LAUNCH;
   }
-  st = launch_decode(plan, ws, st_);
-  if (ws && cudaFreeAsync(ws, st_) != cudaSuccess) st = FA_ERR_LAUNCH;
-  return st;
+  return launch_decode(plan, ws, st_);
+}
+
+extern "C" fa_status fa_sparse_mla_decode_plan(int num_tokens, int num_heads, int topk,
+                                               int* launches, size_t* workspace_bytes) {
+  if (!launches || !workspace_bytes || num_tokens < 0 || topk < 1) return FA_ERR_INVALID_ARG;
+  if (num_heads != 8 && num_heads != 16 && num_heads != 32 && num_heads != 64 &&
+      num_heads != 128)
+    return FA_ERR_UNSUPPORTED;
+  if (topk % 128 != 0 || topk > fa::kDecodeMaxTopk) return FA_ERR_UNSUPPORTED;
+  const int groups = (num_heads + 63) / 64;
+  const int n_tiles = topk / fa::kDecodeKeys;
+  const long long units = (long long)num_tokens * groups;
+  if (units * n_tiles > INT32_MAX) return FA_ERR_UNSUPPORTED;
+  DeviceInfo* dev = nullptr;
+  const fa_status st = device_info(&dev);
+  if (st != FA_OK) return st;
+  *launches = 0;
+  *workspace_bytes = 0;
+  if (num_tokens == 0) return FA_OK;
+  const DecodeSplit d = decode_split(units, n_tiles, dev->sm_count);
+  *launches = d.split && d.grid >= 2 ? 2 : 1;
+  *workspace_bytes = decode_workspace_bytes(d);
+  return FA_OK;
 }
 
 extern "C" fa_status fa_merge_attn_states(void* out, float* out_lse, const void* prefix_out,

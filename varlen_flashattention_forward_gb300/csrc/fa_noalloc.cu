@@ -2,9 +2,12 @@
 // sparse-MLA decode with its partial-result workspace taken from a fixed
 // scratch buffer in device memory instead of an allocation.
 //
-// The buffer is a file-scope __device__ array in its own translation unit,
-// so the device memory is only committed when this module is loaded, on the
-// first call (lazy module loading), not by programs that never call it.
+// The buffer is a file-scope __device__ array in its own translation unit.
+// Under lazy module loading (CUDA_MODULE_LOADING=LAZY, the default since CUDA
+// 12.2) its device memory is committed on a device only when the first call
+// there loads the module; under eager loading, every process that loads the
+// library commits it on every device it uses, whether or not it calls this
+// entry point.
 #include <cstdint>
 #include <mutex>
 
@@ -24,7 +27,8 @@ std::mutex g_mu;
 void* g_scratch[kMaxDevices] = {};
 
 // Device address of the scratch on the current device, looked up once per
-// device with that device current.
+// device with that device current and kept for the life of the process (a
+// cudaDeviceReset invalidates it; the header forbids calls after one).
 fa_status scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_LAUNCH;

@@ -48,6 +48,7 @@
 // prefill.flash_attn", applied to any number of parts.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <cuda.h>
@@ -809,16 +810,18 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeArgs a) {
 template <int NP>
 inline cudaError_t launch_decode_np(const CUtensorMap& map, const DecodeArgs& a,
                                     cudaStream_t stream) {
-  static bool attr_done[64] = {false};
+  // Set once per device; concurrent first calls may both set it (the call
+  // is idempotent), the flag itself is atomic.
+  static std::atomic<bool> attr_done[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev]) {
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(sparse_decode_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kDecodeSmem);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
+    attr_done[dev].store(true, std::memory_order_release);
   }
   sparse_decode_kernel<NP><<<a.grid, kDecodeThreads, kDecodeSmem, stream>>>(map, a);
   e = cudaGetLastError();

@@ -78,6 +78,24 @@ class VarlenWorkload:
         cq, ck = self.cu_seqlens()
         return q, k, v, cq, ck
 
+    def make_inputs_on(self, device):
+        """The same shapes and distributions drawn by a seeded generator on
+        `device` (a different stream of numbers than make_inputs; for timing
+        runs, where drawing gigabytes on the CPU would dominate)."""
+        g = torch.Generator(device=device).manual_seed(self.seed)
+
+        def draw(shape, std):
+            x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+            if std != 1.0:
+                x.mul_(std)
+            return x.to(torch.bfloat16)
+
+        q = draw((self.total_q, self.num_heads, self.d_qk), self.qk_std)
+        k = draw((self.total_k, self.num_heads_k, self.d_qk), self.qk_std)
+        v = draw((self.total_k, self.num_heads_k, self.d_v), self.v_std)
+        cq, ck = self.cu_seqlens()
+        return q, k, v, cq.to(device), ck.to(device)
+
 
 def _randn(shape, g, std):
     """N(0, std^2) drawn in fp32 chunks, rounded to bf16."""
@@ -204,11 +222,15 @@ def small_decode(num_tokens=4, num_heads=64, topk=256, context=1024,
 
 
 VARLEN_BENCH = {
+    "tiny": tiny,
     "vit_full_d80": lambda: vit_full(80),
     "vit_full_d64": lambda: vit_full(64),
     "vit_full_d72": lambda: vit_full(72),
     "vit_full_d128": lambda: vit_full(128),
+    "vit_window_d64": lambda: vit_window(64),
+    "vit_window_d72": lambda: vit_window(72),
     "vit_window_d80": lambda: vit_window(80),
+    "vit_window_d128": lambda: vit_window(128),
     "vit_window64_d80": lambda: vit_window64(80),
     "long_16384": lambda: long_seq(16384),
     "long_36864": lambda: long_seq(36864),
@@ -216,4 +238,47 @@ VARLEN_BENCH = {
     "mla_causal": mla_causal,
     "mla_chunked": mla_chunked,
     "mla_swa": mla_swa,
+}
+
+
+def splitkv_long_k() -> VarlenWorkload:
+    """Few query rows against a long key sequence: one 256-row chunk against
+    65536 keys, 16 heads, d=128 (chunked prefill's context pass, which the
+    vLLM flash_attn page runs non-causal and with the LSE returned:
+    FlashAttnPrefillBackend.run_prefill_context_chunk).  Only 16 query
+    tiles exist for the SMs: the split-KV case."""
+    return VarlenWorkload("splitkv_q256_k65536", [256], [65536], 16, 16, 128, 128,
+                          128 ** -0.5, seed=6)
+
+
+def splitkv_decode_like() -> VarlenWorkload:
+    """One query row per sequence against 32768 keys, 8 sequences, 128 heads,
+    MLA dims (192, 128), bottom-right causal."""
+    return VarlenWorkload("splitkv_q1x8_k32768_mla", [1] * 8, [32768] * 8, 128, 128, 192, 128,
+                          192 ** -0.5, causal=True, seed=7)
+
+
+def gqa_prefill(group: int = 4) -> VarlenWorkload:
+    """Grouped-query attention: 32 query heads over 32/group key/value heads,
+    d=128, 4 x 4096 causal (sglang FA4 PR, "Accuracy Tests": GQA and
+    pack_gqa)."""
+    return VarlenWorkload(f"gqa{group}_causal_4x4096", [4096] * 4, [4096] * 4, 32, 32 // group,
+                          128, 128, 128 ** -0.5, causal=True, seed=8)
+
+
+def gqa_decode_like(group: int = 8) -> VarlenWorkload:
+    """Grouped-query attention with one query row per sequence: 64 sequences
+    against 8192 keys each, 32 query heads over 32/group key/value heads,
+    d=128, bottom-right causal."""
+    return VarlenWorkload(f"gqa{group}_q1x64_k8192", [1] * 64, [8192] * 64, 32, 32 // group,
+                          128, 128, 128 ** -0.5, causal=True, seed=9)
+
+
+# Workloads timed only in the bench's extra block (and covered by parity
+# tests at reduced sizes).
+EXTRA_ONLY = {
+    "splitkv_q256_k65536": splitkv_long_k,
+    "splitkv_q1x8_k32768_mla": splitkv_decode_like,
+    "gqa4_causal_4x4096": lambda: gqa_prefill(4),
+    "gqa8_q1x64_k8192": lambda: gqa_decode_like(8),
 }
