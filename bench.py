@@ -201,7 +201,7 @@ def oracle_sample_rate(w, budget_s: float, seed: int = 0):
 
 
 # ------------------------------------------------------------ GPU timing
-def time_varlen(w, steps, warmup, device, world, on_device=False, e2e=True):
+def time_varlen(w, steps, warmup, device, world, on_device=False, e2e=True, kv_hint=None):
     """CUDA-event times of fa_varlen_fwd on workload w (L2 flushed before each
     step, outside the events), the clocks seen meanwhile, and (e2e) the end
     to end time per step with pinned host inputs copied in and the outputs
@@ -217,7 +217,8 @@ def time_varlen(w, steps, warmup, device, world, on_device=False, e2e=True):
            if w.return_lse else None)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
-    args = (qd, kd, vd, cqd, ckd, max(w.lens_q), max(w.lens_k), w.softmax_scale, w.causal,
+    args = (qd, kd, vd, cqd, ckd, max(w.lens_q),
+            max(w.lens_k) if kv_hint is None else kv_hint, w.softmax_scale, w.causal,
             w.window[0], w.window[1], out, lse)
     for _ in range(warmup):
         fa.fa_varlen_fwd(*args)
@@ -358,6 +359,14 @@ def decode_launches_per_step(d):
     return launches
 
 
+def varlen_plan(w):
+    """[grid, split] of the workload's launch (fa_varlen_fwd_plan)."""
+    import varlen_flashattention_forward_gb300 as fa
+    return list(fa.fa_varlen_fwd_plan(len(w.lens_q), w.total_q, w.total_k, w.num_heads,
+                                      w.num_heads_k, w.d_qk, w.d_v, max(w.lens_k), w.causal,
+                                      *w.window))
+
+
 def _roofline(flops, byts, ms, peaks):
     """Bound, and the fraction of the roofline time (the slower of compute at
     the bf16 peak and bytes at the HBM copy rate) the measured time reaches."""
@@ -391,7 +400,18 @@ def extra_lines(steps, warmup, device, peaks, skip=()):
         bound, frac = _roofline(flops, byts, ms, peaks)
         res[name] = {"ms": round(ms, 4), "ms_min": round(min(t), 4),
                      "tflops": round(flops / ms / 1e9, 1), "gbs": round(byts / ms / 1e6, 1),
-                     "bound": bound, "roofline_frac": round(frac, 4)}
+                     "bound": bound, "roofline_frac": round(frac, 4),
+                     "grid_split": varlen_plan(w)}
+        if name.startswith("splitkv"):
+            # The same call with a max_seqlen_k hint of 1, which keeps the
+            # launch unsplit (the hint steers only the launch shape).
+            try:
+                t1, _, _, _, _ = time_varlen(w, steps, warmup, device, 1, on_device=True,
+                                             e2e=False, kv_hint=1)
+                res[name]["unsplit_ms"] = round(statistics.mean(t1), 4)
+                res[name]["split_speedup"] = round(statistics.mean(t1) / ms, 2)
+            except Exception as exc:
+                res[name]["unsplit_error"] = str(exc)[:200]
         torch.cuda.empty_cache()
     try:
         d = workloads.DecodeWorkload()

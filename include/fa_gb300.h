@@ -104,6 +104,17 @@ typedef enum {
  *   lse           fp32 [num_heads, total_q] natural-log LSE, or NULL.
  *
  * A query row with no visible key gets O = 0 and LSE = -inf.
+ *
+ * Split-KV ([flash_attn] FA4SplitKVCombineKernel): when the work items
+ * (query head x 256 query rows of a sequence) cannot fill half of the SMs
+ * and the keys are long, each item's key tiles are split over a thread-block
+ * cluster of up to 16 CTAs (8 where larger clusters are unavailable).  Each
+ * CTA computes a partial result over its part, and the cluster merges the
+ * partials by their log-sum-exp through distributed shared memory, in a
+ * fixed order: no workspace, and the same result on every run.  The split
+ * is chosen on the host from the sizes and the max_seqlen_k hint (see
+ * fa_varlen_fwd_plan); it changes rounding, never the result beyond it.
+ *
  * Host errors: FA_ERR_INVALID_ARG (null required pointer, negative sizes,
  * batch < 1, head counts, window < -1, scale <= 0, unaligned pointers),
  * FA_ERR_UNSUPPORTED (head dims, batch > 1024), FA_ERR_ARCH.
@@ -115,6 +126,23 @@ fa_status fa_varlen_fwd(const void* q, const void* k, const void* v,
                         int max_seqlen_k, float softmax_scale, int causal,
                         int window_left, int window_right, void* out,
                         float* lse, fa_stream_t stream);
+
+/*
+ * fa_varlen_fwd_plan -- the launch shape fa_varlen_fwd (and
+ * fa_varlen_fwd_strided) would use for a call with these sizes on the
+ * current device, without launching anything.  Arguments as fa_varlen_fwd.
+ *
+ *   *grid   CTAs of the launch (0 when total_q = 0)
+ *   *split  CTAs per work item: 1 = persistent grid of at most one CTA per
+ *           SM walking the work list; > 1 = split-KV, one cluster of
+ *           *split CTAs per work item
+ *
+ * Host errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (head dims, batch),
+ * FA_ERR_ARCH, FA_ERR_LAUNCH (a device query failed).
+ */
+fa_status fa_varlen_fwd_plan(int batch, int total_q, int total_k, int num_heads,
+                             int num_heads_k, int d_qk, int d_v, int max_seqlen_k, int causal,
+                             int window_left, int window_right, int* grid, int* split);
 
 /*
  * fa_varlen_fwd_strided -- fa_varlen_fwd with q, k and v given as strided

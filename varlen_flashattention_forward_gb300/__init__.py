@@ -11,6 +11,8 @@ Entry points (same names as the C ABI):
                 max_seqlen_k, softmax_scale, causal=False, window_left=-1,
                 window_right=-1, out=None, lse=None, return_lse=False,
                 stream=None)
+  fa_varlen_fwd_plan(batch, total_q, total_k, num_heads, num_heads_k, d_qk, d_v,
+                     max_seqlen_k=0, causal=False, window_left=-1, window_right=-1)
   fa_sparse_mla_decode(q, kv_cache, page_table, topk_idx, softmax_scale,
                        out=None, lse=None, return_lse=False, stream=None)
   fa_sparse_mla_decode_plan(num_tokens, num_heads, topk)
@@ -38,7 +40,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
 
 # Exported C symbols (kept in sync with include/fa_gb300.h; a CPU test checks).
-EXPORTS = ("fa_varlen_fwd", "fa_varlen_fwd_strided", "fa_sparse_mla_decode",
+EXPORTS = ("fa_varlen_fwd", "fa_varlen_fwd_plan", "fa_varlen_fwd_strided", "fa_sparse_mla_decode",
            "fa_sparse_mla_decode_plan", "fa_sparse_mla_decode_noalloc", "fa_merge_attn_states",
            "fa_get_device_status", "fa_status_string")
 
@@ -73,6 +75,10 @@ def load_library():
     lib.fa_sparse_mla_decode.argtypes = [p, p, p, p, i32, i32, i32, i32, i32,
                                          f32, p, p, p]
     lib.fa_sparse_mla_decode.restype = i32
+    pi = ctypes.POINTER(i32)
+    lib.fa_varlen_fwd_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                       pi, pi]
+    lib.fa_varlen_fwd_plan.restype = i32
     lib.fa_sparse_mla_decode_plan.argtypes = [i32, i32, i32, ctypes.POINTER(i32),
                                               ctypes.POINTER(ctypes.c_size_t)]
     lib.fa_sparse_mla_decode_plan.restype = i32
@@ -214,6 +220,22 @@ def fa_sparse_mla_decode(q, kv_cache, page_table, topk_idx, softmax_scale=None,
     if st != FA_OK:
         raise FaError(st, "fa_sparse_mla_decode")
     return (out, lse) if lse is not None else out
+
+
+def fa_varlen_fwd_plan(batch, total_q, total_k, num_heads, num_heads_k, d_qk, d_v,
+                       max_seqlen_k=0, causal=False, window_left=-1, window_right=-1):
+    """(grid, split) of an fa_varlen_fwd call of these sizes on the current
+    device: split > 1 means split-KV in clusters of `split` CTAs; see
+    fa_varlen_fwd_plan in include/fa_gb300.h."""
+    lib = load_library()
+    g, s = ctypes.c_int(0), ctypes.c_int(0)
+    st = lib.fa_varlen_fwd_plan(int(batch), int(total_q), int(total_k), int(num_heads),
+                                int(num_heads_k), int(d_qk), int(d_v), int(max_seqlen_k),
+                                int(bool(causal)), int(window_left), int(window_right),
+                                ctypes.byref(g), ctypes.byref(s))
+    if st != FA_OK:
+        raise FaError(st, "fa_varlen_fwd_plan")
+    return g.value, s.value
 
 
 def fa_sparse_mla_decode_plan(num_tokens, num_heads, topk):

@@ -27,12 +27,24 @@
 #include "varlen_fwd_kernel.cuh"
 
 namespace fa {
-cudaError_t launch_varlen_64_64(const VarlenMaps&, const VarlenArgs&, int, cudaStream_t);
-cudaError_t launch_varlen_72_72(const VarlenMaps&, const VarlenArgs&, int, cudaStream_t);
-cudaError_t launch_varlen_80_80(const VarlenMaps&, const VarlenArgs&, int, cudaStream_t);
-cudaError_t launch_varlen_96_96(const VarlenMaps&, const VarlenArgs&, int, cudaStream_t);
-cudaError_t launch_varlen_128_128(const VarlenMaps&, const VarlenArgs&, int, cudaStream_t);
-cudaError_t launch_varlen_192_128(const VarlenMaps&, const VarlenArgs&, int, cudaStream_t);
+cudaError_t launch_varlen_64_64(const VarlenMaps&, const VarlenArgs&, const VarlenLaunch&,
+                                 cudaStream_t);
+cudaError_t plan_varlen_64_64(const VarlenLaunch&, int*, int*);
+cudaError_t launch_varlen_72_72(const VarlenMaps&, const VarlenArgs&, const VarlenLaunch&,
+                                 cudaStream_t);
+cudaError_t plan_varlen_72_72(const VarlenLaunch&, int*, int*);
+cudaError_t launch_varlen_80_80(const VarlenMaps&, const VarlenArgs&, const VarlenLaunch&,
+                                 cudaStream_t);
+cudaError_t plan_varlen_80_80(const VarlenLaunch&, int*, int*);
+cudaError_t launch_varlen_96_96(const VarlenMaps&, const VarlenArgs&, const VarlenLaunch&,
+                                 cudaStream_t);
+cudaError_t plan_varlen_96_96(const VarlenLaunch&, int*, int*);
+cudaError_t launch_varlen_128_128(const VarlenMaps&, const VarlenArgs&, const VarlenLaunch&,
+                                 cudaStream_t);
+cudaError_t plan_varlen_128_128(const VarlenLaunch&, int*, int*);
+cudaError_t launch_varlen_192_128(const VarlenMaps&, const VarlenArgs&, const VarlenLaunch&,
+                                 cudaStream_t);
+cudaError_t plan_varlen_192_128(const VarlenLaunch&, int*, int*);
 }  // namespace fa
 
 // Device status word: bit 0 = a pipeline wait ran out of time.
@@ -161,6 +173,30 @@ fa_status stream_workspace(cudaStream_t stream, size_t need, void** out) {
   return FA_OK;
 }
 
+// Launch shape of a varlen call.  A sequence of l query rows has
+// ceil(l / 256) work items per head, and the sum of the ceilings is at most
+// floor((total_q + 255 batch) / 256), so no more work items than item_bound
+// exist (packed short segments only make fewer).  The KV tiles of one item
+// are estimated from the max_seqlen_k hint (else total_k) and the window;
+// they only steer the split-KV choice, never correctness.
+fa::VarlenLaunch launch_shape(int sm_count, int batch, int total_q, int total_k, int num_heads,
+                              int max_seqlen_k, int causal, int window_left, int window_right) {
+  fa::VarlenLaunch L;
+  L.sm_count = sm_count;
+  L.item_bound = (long long)num_heads *
+                 (((long long)total_q + (long long)(fa::kRowsPerItem - 1) * batch) /
+                  fa::kRowsPerItem);
+  long long kv = total_k;
+  if (max_seqlen_k > 0 && max_seqlen_k < kv) kv = max_seqlen_k;
+  if (window_left >= 0 && (causal || window_right >= 0)) {
+    const long long span =
+        (long long)window_left + (causal ? 0 : window_right) + fa::kRowsPerItem;
+    if (span < kv) kv = span;
+  }
+  L.kv_tiles = (kv + fa::kBN - 1) / fa::kBN;
+  return L;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int tail_width(int d) { return ((d + 15) / 16 * 16) % 64; }
@@ -216,8 +252,8 @@ extern "C" fa_status fa_varlen_fwd_strided(
       !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4) || (lse && !aligned(lse, 4)))
     return FA_ERR_INVALID_ARG;
   if (batch > fa::kMaxBatch) return FA_ERR_UNSUPPORTED;
-  typedef cudaError_t (*Launcher)(const fa::VarlenMaps&, const fa::VarlenArgs&, int,
-                                  cudaStream_t);
+  typedef cudaError_t (*Launcher)(const fa::VarlenMaps&, const fa::VarlenArgs&,
+                                  const fa::VarlenLaunch&, cudaStream_t);
   Launcher launch = nullptr;
   if (d_qk == 64 && d_v == 64) launch = fa::launch_varlen_64_64;
   else if (d_qk == 72 && d_v == 72) launch = fa::launch_varlen_72_72;
@@ -277,14 +313,41 @@ extern "C" fa_status fa_varlen_fwd_strided(
   args.out = static_cast<uint16_t*>(out);
   args.lse = lse;
   args.status = dev->status;
+  args.split = 1;
 
-  // Persistent grid: no more CTAs than SMs or than work items could exist.
-  const int64_t item_bound =
-      (int64_t)num_heads * ((total_q + fa::kRowsPerItem - 1) / fa::kRowsPerItem + batch);
-  int grid = (int)(item_bound < dev->sm_count ? item_bound : dev->sm_count);
-  if (grid < 1) grid = 1;
-  cudaError_t e = launch(maps, args, grid, reinterpret_cast<cudaStream_t>(stream));
+  const fa::VarlenLaunch L = launch_shape(dev->sm_count, batch, total_q, total_k, num_heads,
+                                          max_seqlen_k, causal, window_left, window_right);
+  cudaError_t e = launch(maps, args, L, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+extern "C" fa_status fa_varlen_fwd_plan(int batch, int total_q, int total_k, int num_heads,
+                                        int num_heads_k, int d_qk, int d_v, int max_seqlen_k,
+                                        int causal, int window_left, int window_right,
+                                        int* grid, int* split) {
+  if (!grid || !split) return FA_ERR_INVALID_ARG;
+  if (batch < 1 || total_q < 0 || total_k < 0 || num_heads < 1 || num_heads_k < 1 ||
+      num_heads % num_heads_k != 0 || window_left < -1 || window_right < -1)
+    return FA_ERR_INVALID_ARG;
+  if (batch > fa::kMaxBatch) return FA_ERR_UNSUPPORTED;
+  typedef cudaError_t (*Planner)(const fa::VarlenLaunch&, int*, int*);
+  Planner plan = nullptr;
+  if (d_qk == 64 && d_v == 64) plan = fa::plan_varlen_64_64;
+  else if (d_qk == 72 && d_v == 72) plan = fa::plan_varlen_72_72;
+  else if (d_qk == 80 && d_v == 80) plan = fa::plan_varlen_80_80;
+  else if (d_qk == 96 && d_v == 96) plan = fa::plan_varlen_96_96;
+  else if (d_qk == 128 && d_v == 128) plan = fa::plan_varlen_128_128;
+  else if (d_qk == 192 && d_v == 128) plan = fa::plan_varlen_192_128;
+  if (!plan) return FA_ERR_UNSUPPORTED;
+  DeviceInfo* dev = nullptr;
+  const fa_status st = device_info(&dev);
+  if (st != FA_OK) return st;
+  *grid = 0;
+  *split = 1;
+  if (total_q == 0) return FA_OK;
+  const fa::VarlenLaunch L = launch_shape(dev->sm_count, batch, total_q, total_k, num_heads,
+                                          max_seqlen_k, causal, window_left, window_right);
+  return plan(L, grid, split) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 namespace {

@@ -48,7 +48,9 @@
 // persistent scheduler).
 #pragma once
 
+#include <atomic>
 #include <cstdint>
+#include <cstring>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -185,6 +187,11 @@ struct VarlenArgs {
   uint16_t* out;     // bf16 [total_q, H, d_v]
   float* lse;        // [H, total_q] or null
   unsigned int* status;
+  // Split-KV: CTAs per work item (the cluster size; 1 = no split).  With
+  // split > 1 the grid holds one cluster per work item; rank r of a cluster
+  // runs part r of the item's KV tiles and the cluster combines the parts
+  // (split_combine).
+  int split;
 };
 
 struct VarlenMaps {
@@ -322,7 +329,8 @@ __device__ __forceinline__ void issue_pv_half(uint32_t o, uint32_t p, uint64_t v
 // packed ViT mix (6 images, 256 to 9216 tokens, 16 heads) the busiest CTA then
 // carries 1.04x the mean work instead of 1.07x with a plain round robin;
 // causal 4 x 4096: 1.01x instead of 1.14x.
-__device__ __forceinline__ int snake_item(int round) {
+__device__ __forceinline__ int snake_item(int round, int split) {
+  if (split > 1) return round == 0 ? (int)blockIdx.x / split : 0x7fffffff;  // one item per cluster
   const int g = (int)gridDim.x, b = (int)blockIdx.x;
   return round * g + ((round & 1) ? g - 1 - b : b);
 }
@@ -506,7 +514,8 @@ static __device__ __noinline__ void build_work_list(const int* cu_q, const int* 
 }
 
 __device__ __forceinline__ WorkItem decode_item(int it, const VarlenArgs& a,
-                                                const int* s_prefix, const int* s_sorted) {
+                                                const int* s_prefix, const int* s_sorted,
+                                                int split = 1) {
   // Largest sorted position p with prefix[p] <= it (skips empty sequences).
   int lo = 0, hi = a.batch - 1;
   while (lo < hi) {
@@ -539,14 +548,124 @@ __device__ __forceinline__ WorkItem decode_item(int it, const VarlenArgs& a,
     w.tile_lo = key_lo / kBN;
     w.n_kv = (key_hi + kBN - 1) / kBN - w.tile_lo;
   }
+  if (split > 1) {
+    // Split-KV: this CTA's part of the item's KV tiles (its rank in the
+    // cluster; parts differ in size by at most one tile, and may be empty).
+    const int part = (int)blockIdx.x % split;
+    const int p0 = w.n_kv * part / split;
+    const int p1 = w.n_kv * (part + 1) / split;
+    w.tile_lo += p0;
+    w.n_kv = p1 - p0;
+  }
   return w;
 }
 
+// ------------------------------------------------------------ split-KV combine
+// Split-KV partials in shared memory, in the Q tiles and K/V rings of the
+// item's CTAs (dead once the item's last MMA is done): row r of the item's
+// 256 rows holds its unnormalised O (d_v fp32; 16 bytes of padding put the
+// rows of a warp in different banks), then every row's (m, l) with m the
+// running maximum in scaled log2 units, then the combining CTA's per-row
+// weights of the parts.
+constexpr int kMaxSplit = 16;
+template <int D_V>
+struct SplitStash {
+  static constexpr int kRowBytes = D_V * 4 + 16;
+  static constexpr int kMlOff = kRowsPerItem * kRowBytes;
+  static constexpr int kWOff = kMlOff + kRowsPerItem * 8;
+  static constexpr int kBytes = kWOff + kRowsPerItem * kMaxSplit * 4;
+};
+
+// The combine of one work item's parts, run by every thread of each CTA of
+// the item's cluster once all of them have left their pipelines.  Rank r of
+// S combines rows [r n / S, (r + 1) n / S) of the item's n rows, reading every
+// part's row through distributed shared memory, in rank order:
+//   M = max_s m_s,  w_s = 2^(m_s - M),  L = sum_s w_s l_s,
+//   O = sum_s (w_s / L) O_s,  LSE = ln 2 (M + log2 L)
+// (the LSE-weighted merge of split-KV partials of the vLLM flash_attn page,
+// FA4SplitKVCombineKernel).  A row with no key in any part gets O = 0 and
+// LSE = -inf.
+template <int D_V>
+static __device__ __noinline__ void split_combine(const VarlenArgs args, uint8_t* smem,
+                                                  const int* s_prefix, const int* s_sorted,
+                                                  int total_items) {
+  using St = SplitStash<D_V>;
+  const int S = args.split;
+  const int rank = (int)blockIdx.x % S;
+  const int it = (int)blockIdx.x / S;
+  ptx::cluster_arrive_release();
+  ptx::cluster_wait_acquire();  // every part is in its CTA's shared memory
+  if (it < total_items) {
+    const WorkItem w = decode_item(it, args, s_prefix, s_sorted, S);
+    const int rows = min(kRowsPerItem, w.lq - w.row0);
+    const int r_lo = rows * rank / S, r_hi = rows * (rank + 1) / S;
+    const uint32_t base = ptx::smem_u32(smem);
+    float* wgt = reinterpret_cast<float*>(smem + St::kWOff);
+    const float neg_inf = -__int_as_float(0x7f800000);
+    for (int r = r_lo + (int)threadIdx.x; r < r_hi; r += (int)blockDim.x) {
+      float* wr = wgt + (r - r_lo) * kMaxSplit;
+      float M = neg_inf;
+      for (int sp = 0; sp < S; ++sp) {
+        const float2 ml = ptx::ld_shared_cluster_v2(ptx::mapa_shared(base + St::kMlOff + r * 8, sp));
+        wr[sp] = ml.y > 0.f ? ml.x : neg_inf;  // parts with no key of this row: weight 0
+        M = fmaxf(M, wr[sp]);
+      }
+      float L = 0.f;
+      for (int sp = 0; sp < S; ++sp) {
+        const float2 ml = ptx::ld_shared_cluster_v2(ptx::mapa_shared(base + St::kMlOff + r * 8, sp));
+        const float e = wr[sp] == neg_inf ? 0.f : ptx::ex2(wr[sp] - M);
+        wr[sp] = e;
+        L += e * ml.y;
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      for (int sp = 0; sp < S; ++sp) wr[sp] *= inv;
+      if (args.lse) {
+        const size_t tok = (size_t)(w.q_start + w.row0 + r);
+        args.lse[(size_t)w.head * args.total_q + tok] =
+            L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : neg_inf;
+      }
+    }
+    __syncthreads();
+    constexpr int kGroups = D_V / 8;  // 8 output columns (16 bytes of bf16) per unit
+    const int units = (r_hi - r_lo) * kGroups;
+    for (int u = (int)threadIdx.x; u < units; u += (int)blockDim.x) {
+      const int rr = u / kGroups, g = u - rr * kGroups;
+      const int r = r_lo + rr;
+      const float* wr = wgt + rr * kMaxSplit;
+      float acc[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[c] = 0.f;
+      for (int sp = 0; sp < S; ++sp) {
+        const float ws = wr[sp];
+        if (ws == 0.f) continue;
+        const uint32_t a = ptx::mapa_shared(base + r * St::kRowBytes + g * 32, sp);
+        const float4 v0 = ptx::ld_shared_cluster_v4(a);
+        const float4 v1 = ptx::ld_shared_cluster_v4(a + 16);
+        acc[0] += ws * v0.x; acc[1] += ws * v0.y; acc[2] += ws * v0.z; acc[3] += ws * v0.w;
+        acc[4] += ws * v1.x; acc[5] += ws * v1.y; acc[6] += ws * v1.z; acc[7] += ws * v1.w;
+      }
+      const size_t tok = (size_t)(w.q_start + w.row0 + r);
+      uint4 pk;
+      pk.x = ptx::pack_bf16x2(acc[0], acc[1]);
+      pk.y = ptx::pack_bf16x2(acc[2], acc[3]);
+      pk.z = ptx::pack_bf16x2(acc[4], acc[5]);
+      pk.w = ptx::pack_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(args.out + (tok * args.num_heads + w.head) * (size_t)D_V + 8 * g) = pk;
+    }
+  }
+  ptx::cluster_arrive_release();
+  ptx::cluster_wait_acquire();  // no CTA leaves while another still reads its shared memory
+}
+
 // ------------------------------------------------------------ the kernel
-template <int D_QK, int D_V>
+// kSplit selects the split-KV instantiation (launched in clusters of
+// args.split CTAs); the other one compiles without any split-KV code, whose
+// extra state would otherwise cost the pipeline loops registers.
+template <int D_QK, int D_V, bool kSplit>
 __global__ void __launch_bounds__(kVarlenThreads, 1)
     varlen_fwd_kernel(const __grid_constant__ VarlenMaps maps, const VarlenArgs args) {
   using C = VarlenCfg<D_QK, D_V>;
+  const int split = kSplit ? args.split : 1;
   using QK = typename C::QK;
   using VD = typename C::VD;
   constexpr int NK = C::nk, NV = C::nv;
@@ -609,6 +728,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
   }
   static_assert(NK * C::k_slot_bytes >= 3 * kMaxBatch * (int)sizeof(int),
                 "the K ring holds the work-list scratch");
+  static_assert(SplitStash<D_V>::kBytes <= 2 * C::q_pairs * C::q_tile_bytes +
+                                               NK * C::k_slot_bytes + NV * C::v_slot_bytes,
+                "the split-KV partials fit in the Q tiles and K/V rings");
   build_work_list(args.cu_q, args.cu_k, args.batch, args.num_heads, s_prefix, s_sorted, s_part,
                   reinterpret_cast<int*>(k_ring));  // ends with __syncthreads
   ptx::tc_fence_before();
@@ -631,9 +753,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         uint32_t kn = 0, vn = 0;
         bool ok = true;
         for (int r = 0; r * (int)gridDim.x < total_items && ok; ++r) {
-          const int it = snake_item(r);
+          const int it = snake_item(r, split);
           if (it >= total_items) continue;
-          const WorkItem w = decode_item(it, args, s_prefix, s_sorted);
+          const WorkItem w = decode_item(it, args, s_prefix, s_sorted, split);
           if (w.n_kv == 0) continue;
           const int pair = C::q_pairs == 2 ? (int)(item_n & 1) : 0;
           ++item_n;
@@ -773,9 +895,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         // the ring); an issuer whose tile is absent from the item only waits
         // and releases.
         for (int r = 0; r * (int)gridDim.x < total_items && ok; ++r) {
-          const int it = snake_item(r);
+          const int it = snake_item(r, split);
           if (it >= total_items) continue;
-          const WorkItem w = decode_item(it, args, s_prefix, s_sorted);
+          const WorkItem w = decode_item(it, args, s_prefix, s_sorted, split);
           if (w.n_kv == 0) continue;
           const bool mine = t < w.n_qt;
           const int qb = 2 * (C::q_pairs == 2 ? (int)(item_n & 1) : 0) + t;  // Q buffer
@@ -901,9 +1023,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     bool ok = true;
 
     for (int r = 0; r * (int)gridDim.x < total_items && ok; ++r) {
-      const int it = snake_item(r);
+      const int it = snake_item(r, split);
       if (it >= total_items) continue;
-      const WorkItem w = decode_item(it, args, s_prefix, s_sorted);
+      const WorkItem w = decode_item(it, args, s_prefix, s_sorted, split);
       const int qb = 2 * (C::q_pairs == 2 ? (int)(item_n & 1) : 0) + t;  // this item's Q buffer
       if (w.n_kv > 0) ++item_n;
       if (t >= w.n_qt) continue;
@@ -1038,6 +1160,22 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
       }
       if (!ok) break;
 
+      if (kSplit) {
+        // Split-KV: this CTA holds one part of the item.  Its O stays in
+        // TMEM for the cluster combine, and (m, l) go into the row's first
+        // two S/P columns, dead once the last P V (before o_full) is done.
+        if (w.n_kv > 0) {
+          ok = wait_warp(ptx::smem_u32(&cb->o_full[t]), on & 1, abort_flag, args.status);
+          ++on;
+          if (!ok) break;
+          ptx::tc_fence_after();
+          const uint32_t ml[2] = {__float_as_uint(m_used), __float_as_uint(l)};
+          ptx::tmem_st2(s_addr, ml);
+          ptx::tmem_wait_st();
+        }
+        continue;
+      }
+
       // ---- epilogue: O / l -> bf16 rows, LSE
       uint32_t o[C::pv_n];
       if (w.n_kv > 0) {
@@ -1105,10 +1243,53 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     }
     release_staged();
     ptx::bulk_wait_all();  // every O row written before the CTA exits
+    if (kSplit) {
+      // Both warpgroups are past their last O wait, so every MMA of the item
+      // has completed (each issuer's last commit covers all of its MMAs) and
+      // the Q tiles and K/V rings are dead: the partial goes there.
+      ptx::named_bar_sync_n(1, 256);
+      const int it = (int)blockIdx.x / split;
+      const WorkItem w = it < total_items ? decode_item(it, args, s_prefix, s_sorted, split) : WorkItem{};
+      if (it < total_items && t < w.n_qt) {
+        ptx::tc_fence_after();
+        const int r = t * kBM + row_in_tile;  // row within the item
+        uint8_t* row = smem + r * SplitStash<D_V>::kRowBytes;
+        const bool has_o = w.n_kv > 0;
+        float sp_m = neg_inf, sp_l = 0.f;
+        if (has_o) {
+          uint32_t ml[2];
+          ptx::tmem_ld2(s_addr, ml);
+          ptx::tmem_wait_ld();
+          sp_m = __uint_as_float(ml[0]);
+          sp_l = __uint_as_float(ml[1]);
+        }
+        if (has_o) {
+#pragma unroll
+          for (int c0 = 0; c0 < D_V; c0 += 16) {
+            uint32_t o[16];
+            ptx::tmem_ld16(o_addr + c0, o);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence16(o);
+#pragma unroll
+            for (int c = 0; c < 16; c += 4)
+              if (c0 + c < D_V)
+                *reinterpret_cast<uint4*>(row + (c0 + c) * 4) =
+                    make_uint4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < D_V; c += 4)
+            *reinterpret_cast<uint4*>(row + c * 4) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        *reinterpret_cast<float2*>(smem + SplitStash<D_V>::kMlOff + r * 8) =
+            make_float2(sp_m, sp_l);
+      }
+    }
   }
 
   ptx::tc_fence_before();
   __syncthreads();
+  if (kSplit) split_combine<D_V>(args, smem, s_prefix, s_sorted, total_items);
   if (warp == kMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
@@ -1124,26 +1305,132 @@ inline size_t varlen_smem_bytes(int batch) {
          sizeof(VarlenBarriers) + 8 * (size_t)(batch + 1) + 4 * kVarlenThreads + 16;
 }
 
-// Launches one instantiation.  The dynamic shared-memory limit is raised once
-// per device to the size needed for the largest supported batch.
+// What the host knows about a call's work, for the launch shape.
+struct VarlenLaunch {
+  int sm_count;
+  long long item_bound;  // upper bound on the work items (query heads x 256-row pairs)
+  long long kv_tiles;    // estimate of one item's KV tiles (performance only)
+};
+
+// Largest number of clusters of `split` CTAs of this kernel that can be
+// resident at once on the current device (0 if none), queried once per
+// device and cluster size.
 template <int D_QK, int D_V>
-cudaError_t launch_varlen_impl(const VarlenMaps& maps, const VarlenArgs& args, int grid,
-                               cudaStream_t stream) {
-  static bool attr_done[64] = {false};
+int varlen_max_clusters(int dev, int split) {
+  static std::atomic<int> cache[64][kMaxSplit + 1];  // value + 1; 0 = not yet queried
+  const int c = cache[dev][split].load(std::memory_order_acquire);
+  if (c > 0) return c - 1;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(split);
+  cfg.blockDim = dim3(kVarlenThreads);
+  cfg.dynamicSmemBytes = varlen_smem_bytes<D_QK, D_V>(kMaxBatch);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, varlen_fwd_kernel<D_QK, D_V, true>, &cfg) != cudaSuccess) {
+    cudaGetLastError();  // not a sticky error: clear it and report no cluster
+    n = 0;
+  }
+  cache[dev][split].store(n + 1, std::memory_order_release);
+  return n;
+}
+
+// Split-KV when the work items cannot fill half of the SMs: the largest
+// cluster size (at most kMaxSplit, 8 where larger clusters are unavailable)
+// whose clusters, one per item, are all resident at once and whose parts
+// keep at least four KV tiles.  1 = no split.
+template <int D_QK, int D_V>
+int varlen_split_choice(int dev, const VarlenLaunch& L, bool large_clusters) {
+  if (L.item_bound < 1 || L.item_bound * 2 > L.sm_count || L.kv_tiles < 8) return 1;
+  for (int s = large_clusters ? kMaxSplit : 8; s >= 2; --s) {
+    if (L.kv_tiles < 4LL * s || L.item_bound * s > L.sm_count) continue;
+    if (L.item_bound <= varlen_max_clusters<D_QK, D_V>(dev, s)) return s;
+  }
+  return 1;
+}
+
+// Launch shape the launcher below picks: CTAs and CTAs per work item.
+template <int D_QK, int D_V>
+cudaError_t varlen_plan_impl(const VarlenLaunch& L, int* grid, int* split) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev]) {
-    e = cudaFuncSetAttribute(varlen_fwd_kernel<D_QK, D_V>,
+  // Without the non-portable cluster-size permission set (the launcher sets
+  // it on first use) the query still reports what is possible.
+  cudaFuncSetAttribute(varlen_fwd_kernel<D_QK, D_V, true>,
+                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)varlen_smem_bytes<D_QK, D_V>(kMaxBatch));
+  const bool large = cudaFuncSetAttribute(varlen_fwd_kernel<D_QK, D_V, true>,
+                                          cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                          1) == cudaSuccess;
+  cudaGetLastError();
+  *split = varlen_split_choice<D_QK, D_V>(dev, L, large);
+  long long g = *split > 1 ? L.item_bound * *split
+                           : (L.item_bound < L.sm_count ? L.item_bound : L.sm_count);
+  *grid = (int)(g < 1 ? 1 : g);
+  return cudaSuccess;
+}
+
+// Launches one instantiation: a persistent grid of at most one CTA per SM,
+// or, for split-KV, one cluster per work item.  The dynamic shared-memory
+// limit (for the largest supported batch) and the cluster-size permission
+// are set once per device; concurrent first calls may both set them (the
+// calls are idempotent), the flags themselves are atomic.
+template <int D_QK, int D_V>
+cudaError_t launch_varlen_impl(const VarlenMaps& maps, const VarlenArgs& args_in,
+                               const VarlenLaunch& L, cudaStream_t stream) {
+  static std::atomic<int> attr_done[64];  // 0 = not set, 1 = set, 2 = set with large clusters
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int attrs = attr_done[dev].load(std::memory_order_acquire);
+  if (attrs == 0) {
+    e = cudaFuncSetAttribute(varlen_fwd_kernel<D_QK, D_V, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)varlen_smem_bytes<D_QK, D_V>(kMaxBatch));
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
+    e = cudaFuncSetAttribute(varlen_fwd_kernel<D_QK, D_V, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)varlen_smem_bytes<D_QK, D_V>(kMaxBatch));
+    if (e != cudaSuccess) return e;
+    const bool large = cudaFuncSetAttribute(varlen_fwd_kernel<D_QK, D_V, true>,
+                                            cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                            1) == cudaSuccess;
+    if (!large) cudaGetLastError();
+    attrs = large ? 2 : 1;
+    attr_done[dev].store(attrs, std::memory_order_release);
   }
+  VarlenArgs args = args_in;
+  args.split = varlen_split_choice<D_QK, D_V>(dev, L, attrs == 2);
   const size_t smem = varlen_smem_bytes<D_QK, D_V>(args.batch);
-  varlen_fwd_kernel<D_QK, D_V><<<grid, kVarlenThreads, smem, stream>>>(maps, args);
-  return cudaGetLastError();
+  if (args.split == 1) {
+    long long grid = L.item_bound < L.sm_count ? L.item_bound : L.sm_count;
+    if (grid < 1) grid = 1;
+    varlen_fwd_kernel<D_QK, D_V, false><<<(int)grid, kVarlenThreads, smem, stream>>>(maps, args);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3((unsigned)(L.item_bound * args.split));
+  cfg.blockDim = dim3(kVarlenThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = args.split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, varlen_fwd_kernel<D_QK, D_V, true>, maps, args);
 }
 
 }  // namespace fa
@@ -1151,7 +1438,10 @@ cudaError_t launch_varlen_impl(const VarlenMaps& maps, const VarlenArgs& args, i
 #define FA_DEFINE_VARLEN_LAUNCHER(DQK, DV)                                              \
   namespace fa {                                                                         \
   cudaError_t launch_varlen_##DQK##_##DV(const VarlenMaps& maps, const VarlenArgs& args, \
-                                         int grid, cudaStream_t stream) {               \
-    return launch_varlen_impl<DQK, DV>(maps, args, grid, stream);                        \
+                                         const VarlenLaunch& L, cudaStream_t stream) {  \
+    return launch_varlen_impl<DQK, DV>(maps, args, L, stream);                           \
+  }                                                                                      \
+  cudaError_t plan_varlen_##DQK##_##DV(const VarlenLaunch& L, int* grid, int* split) {   \
+    return varlen_plan_impl<DQK, DV>(L, grid, split);                                    \
   }                                                                                      \
   }
