@@ -653,6 +653,7 @@ static __device__ __noinline__ void split_combine(const VarlenArgs args, uint8_t
       *reinterpret_cast<uint4*>(args.out + (tok * args.num_heads + w.head) * (size_t)D_V + 8 * g) = pk;
     }
   }
+  __syncwarp();
   ptx::cluster_arrive_release();
   ptx::cluster_wait_acquire();  // no CTA leaves while another still reads its shared memory
 }
