@@ -201,7 +201,8 @@ def oracle_sample_rate(w, budget_s: float, seed: int = 0):
 
 
 # ------------------------------------------------------------ GPU timing
-def time_varlen(w, steps, warmup, device, world, on_device=False, e2e=True, kv_hint=None):
+def time_varlen(w, steps, warmup, device, world, on_device=False, e2e=True, kv_hint=None,
+                q_hint=None):
     """CUDA-event times of fa_varlen_fwd on workload w (L2 flushed before each
     step, outside the events), the clocks seen meanwhile, and (e2e) the end
     to end time per step with pinned host inputs copied in and the outputs
@@ -217,7 +218,7 @@ def time_varlen(w, steps, warmup, device, world, on_device=False, e2e=True, kv_h
            if w.return_lse else None)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
-    args = (qd, kd, vd, cqd, ckd, max(w.lens_q),
+    args = (qd, kd, vd, cqd, ckd, max(w.lens_q) if q_hint is None else q_hint,
             max(w.lens_k) if kv_hint is None else kv_hint, w.softmax_scale, w.causal,
             w.window[0], w.window[1], out, lse)
     for _ in range(warmup):
@@ -359,12 +360,13 @@ def decode_launches_per_step(d):
     return launches
 
 
-def varlen_plan(w):
-    """[grid, split] of the workload's launch (fa_varlen_fwd_plan)."""
+def varlen_plan(w, q_hint=None, kv_hint=None):
+    """[grid, split, heads_per_tile] of the workload's launch (fa_varlen_fwd_plan)."""
     import varlen_flashattention_forward_gb300 as fa
-    return list(fa.fa_varlen_fwd_plan(len(w.lens_q), w.total_q, w.total_k, w.num_heads,
-                                      w.num_heads_k, w.d_qk, w.d_v, max(w.lens_k), w.causal,
-                                      *w.window))
+    return list(fa.fa_varlen_fwd_plan(
+        len(w.lens_q), w.total_q, w.total_k, w.num_heads, w.num_heads_k, w.d_qk, w.d_v,
+        max(w.lens_q) if q_hint is None else q_hint,
+        max(w.lens_k) if kv_hint is None else kv_hint, w.causal, *w.window))
 
 
 def _roofline(flops, byts, ms, peaks):
@@ -412,6 +414,17 @@ def extra_lines(steps, warmup, device, peaks, skip=()):
                 res[name]["split_speedup"] = round(statistics.mean(t1) / ms, 2)
             except Exception as exc:
                 res[name]["unsplit_error"] = str(exc)[:200]
+        if name.startswith("gqa"):
+            # The same call with a max_seqlen_q hint large enough that no
+            # heads are packed (the hint steers only the launch shape).
+            try:
+                t1, _, _, _, _ = time_varlen(w, steps, warmup, device, 1, on_device=True,
+                                             e2e=False, q_hint=1 << 20)
+                res[name]["unpacked_ms"] = round(statistics.mean(t1), 4)
+                res[name]["unpacked_grid_split"] = varlen_plan(w, q_hint=1 << 20)
+                res[name]["pack_speedup"] = round(statistics.mean(t1) / ms, 2)
+            except Exception as exc:
+                res[name]["unpacked_error"] = str(exc)[:200]
         torch.cuda.empty_cache()
     try:
         d = workloads.DecodeWorkload()

@@ -89,10 +89,18 @@ typedef enum {
  *   cu_seqlens_k  int32 [batch + 1] device, same for keys/values.
  *   batch         1 .. 1024
  *   num_heads, num_heads_k  num_heads % num_heads_k == 0; query head h reads
- *                 key/value head h / (num_heads / num_heads_k).
+ *                 key/value head h / (num_heads / num_heads_k).  When the
+ *                 query sequences are short (by the max_seqlen_q hint, else
+ *                 total_q / batch), P query heads of one group share each
+ *                 128-row query tile (head-group packing, [sglang-fa4]
+ *                 "Accuracy Tests": pack_gqa), so that each K/V tile is
+ *                 loaded once for P heads; P is the largest power of two up
+ *                 to 16 that divides the group and leaves each work item
+ *                 (256 / P tokens) at least the expected query length.
  *   (d_qk, d_v)   one of (64,64) (72,72) (80,80) (96,96) (128,128) (192,128).
  *   max_seqlen_q, max_seqlen_k  host hints only (never used for
- *                 correctness; may be 0).
+ *                 correctness; may be 0): they steer head-group packing
+ *                 and split-KV.
  *   softmax_scale scale applied to Q Kᵀ before the softmax (> 0).
  *   causal        nonzero: key j is visible to query row i of a sequence iff
  *                 j <= i + (Lk - Lq), i.e. the diagonal is aligned to the
@@ -136,13 +144,16 @@ fa_status fa_varlen_fwd(const void* q, const void* k, const void* v,
  *   *split  CTAs per work item: 1 = persistent grid of at most one CTA per
  *           SM walking the work list; > 1 = split-KV, one cluster of
  *           *split CTAs per work item
+ *   *heads_per_tile  query heads packed into one 128-row query tile (GQA
+ *           head-group packing): 1, or P in {2, 4, 8, 16}
  *
  * Host errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (head dims, batch),
  * FA_ERR_ARCH, FA_ERR_LAUNCH (a device query failed).
  */
 fa_status fa_varlen_fwd_plan(int batch, int total_q, int total_k, int num_heads,
-                             int num_heads_k, int d_qk, int d_v, int max_seqlen_k, int causal,
-                             int window_left, int window_right, int* grid, int* split);
+                             int num_heads_k, int d_qk, int d_v, int max_seqlen_q,
+                             int max_seqlen_k, int causal, int window_left, int window_right,
+                             int* grid, int* split, int* heads_per_tile);
 
 /*
  * fa_varlen_fwd_strided -- fa_varlen_fwd with q, k and v given as strided

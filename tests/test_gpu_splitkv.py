@@ -18,8 +18,9 @@ pytestmark = pytest.mark.gpu
 
 
 def plan(lens_q, lens_k, H, Hk, dqk, dv, causal=False, wl=-1, wr=-1):
-    return fa.fa_varlen_fwd_plan(len(lens_q), sum(lens_q), sum(lens_k), H, Hk, dqk, dv, 0,
-                                 causal, wl, wr)
+    grid, split, _ = fa.fa_varlen_fwd_plan(len(lens_q), sum(lens_q), sum(lens_k), H, Hk, dqk,
+                                           dv, 0, 0, causal, wl, wr)
+    return grid, split
 
 
 def check(lens_q, lens_k, H, Hk, dqk, dv, seed, causal=False, wl=-1, wr=-1, want_split=True):

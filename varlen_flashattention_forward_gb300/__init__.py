@@ -12,7 +12,8 @@ Entry points (same names as the C ABI):
                 window_right=-1, out=None, lse=None, return_lse=False,
                 stream=None)
   fa_varlen_fwd_plan(batch, total_q, total_k, num_heads, num_heads_k, d_qk, d_v,
-                     max_seqlen_k=0, causal=False, window_left=-1, window_right=-1)
+                     max_seqlen_q=0, max_seqlen_k=0, causal=False, window_left=-1,
+                     window_right=-1)
   fa_sparse_mla_decode(q, kv_cache, page_table, topk_idx, softmax_scale,
                        out=None, lse=None, return_lse=False, stream=None)
   fa_sparse_mla_decode_plan(num_tokens, num_heads, topk)
@@ -77,7 +78,7 @@ def load_library():
     lib.fa_sparse_mla_decode.restype = i32
     pi = ctypes.POINTER(i32)
     lib.fa_varlen_fwd_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
-                                       pi, pi]
+                                       i32, pi, pi, pi]
     lib.fa_varlen_fwd_plan.restype = i32
     lib.fa_sparse_mla_decode_plan.argtypes = [i32, i32, i32, ctypes.POINTER(i32),
                                               ctypes.POINTER(ctypes.c_size_t)]
@@ -223,19 +224,22 @@ def fa_sparse_mla_decode(q, kv_cache, page_table, topk_idx, softmax_scale=None,
 
 
 def fa_varlen_fwd_plan(batch, total_q, total_k, num_heads, num_heads_k, d_qk, d_v,
-                       max_seqlen_k=0, causal=False, window_left=-1, window_right=-1):
-    """(grid, split) of an fa_varlen_fwd call of these sizes on the current
-    device: split > 1 means split-KV in clusters of `split` CTAs; see
-    fa_varlen_fwd_plan in include/fa_gb300.h."""
+                       max_seqlen_q=0, max_seqlen_k=0, causal=False, window_left=-1,
+                       window_right=-1):
+    """(grid, split, heads_per_tile) of an fa_varlen_fwd call of these sizes
+    on the current device: split > 1 means split-KV in clusters of `split`
+    CTAs, heads_per_tile > 1 GQA head-group packing; see fa_varlen_fwd_plan
+    in include/fa_gb300.h."""
     lib = load_library()
-    g, s = ctypes.c_int(0), ctypes.c_int(0)
+    g, s, p = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
     st = lib.fa_varlen_fwd_plan(int(batch), int(total_q), int(total_k), int(num_heads),
-                                int(num_heads_k), int(d_qk), int(d_v), int(max_seqlen_k),
-                                int(bool(causal)), int(window_left), int(window_right),
-                                ctypes.byref(g), ctypes.byref(s))
+                                int(num_heads_k), int(d_qk), int(d_v), int(max_seqlen_q),
+                                int(max_seqlen_k), int(bool(causal)), int(window_left),
+                                int(window_right), ctypes.byref(g), ctypes.byref(s),
+                                ctypes.byref(p))
     if st != FA_OK:
         raise FaError(st, "fa_varlen_fwd_plan")
-    return g.value, s.value
+    return g.value, s.value, p.value
 
 
 def fa_sparse_mla_decode_plan(num_tokens, num_heads, topk):

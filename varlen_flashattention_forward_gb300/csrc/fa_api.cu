@@ -111,17 +111,19 @@ EncodeTiledFn encode_fn() {
 }
 
 // 3-D bf16 tensor [tokens, heads, dim] (dim innermost) viewed through a box of
-// {box_w, 1, box_rows}.  The swizzle matches the box width (64 -> 128 B,
-// 32 -> 64 B, 16 -> 32 B).  Elements past `dim` or `tokens` read as zero.
+// {box_w, box_heads, box_rows}: shared-memory row r of a box is token
+// r / box_heads, head r % box_heads.  The swizzle matches the box width
+// (64 -> 128 B, 32 -> 64 B, 16 -> 32 B).  Elements past `dim` or `tokens`
+// read as zero.
 bool encode_rows(CUtensorMap* m, const void* base, int dim, int heads, int tokens, int box_w,
-                 int box_rows, long long head_stride, long long row_stride) {
+                 int box_rows, long long head_stride, long long row_stride, int box_heads = 1) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)dim, (cuuint64_t)heads,
                         (cuuint64_t)(tokens > 0 ? tokens : 1)};
   // Strides in bytes of the head and token dimensions (elements are bf16).
   cuuint64_t strides[2] = {(cuuint64_t)head_stride * 2, (cuuint64_t)row_stride * 2};
-  cuuint32_t box[3] = {(cuuint32_t)box_w, 1u, (cuuint32_t)box_rows};
+  cuuint32_t box[3] = {(cuuint32_t)box_w, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUtensorMapSwizzle swz = box_w == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
                            : box_w == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -174,18 +176,36 @@ fa_status stream_workspace(cudaStream_t stream, size_t need, void** out) {
 }
 
 // Launch shape of a varlen call.  A sequence of l query rows has
-// ceil(l / 256) work items per head, and the sum of the ceilings is at most
-// floor((total_q + 255 batch) / 256), so no more work items than item_bound
-// exist (packed short segments only make fewer).  The KV tiles of one item
+// ceil(l / t) work items per head group (t = 256 / P tokens per item, P
+// heads per group), and the sum of the ceilings is at most
+// floor((total_q + (t - 1) batch) / t), so no more work items than
+// item_bound exist (packed short segments only make fewer).  The KV tiles of one item
 // are estimated from the max_seqlen_k hint (else total_k) and the window;
 // they only steer the split-KV choice, never correctness.
+// GQA head-group packing factor (log2): the largest power of two P <= 16
+// that divides the group size num_heads / num_heads_k and still leaves a
+// work item (256 / P tokens) at least as many tokens as a sequence is
+// expected to have (the max_seqlen_q hint, else the mean).  Short query
+// sequences then share each K/V tile among P heads instead of loading it
+// once per head; long ones gain nothing from it and stay unpacked.
+int pack_shift_for(int batch, int total_q, int num_heads, int num_heads_k, int max_seqlen_q) {
+  const int g = num_heads / num_heads_k;
+  long long lq = max_seqlen_q > 0 ? max_seqlen_q : ((long long)total_q + batch - 1) / batch;
+  if (lq < 1) lq = 1;
+  int shift = 0;
+  while (shift < 4 && g % (2 << shift) == 0 && (fa::kRowsPerItem >> (shift + 1)) >= lq) ++shift;
+  return shift;
+}
+
 fa::VarlenLaunch launch_shape(int sm_count, int batch, int total_q, int total_k, int num_heads,
-                              int max_seqlen_k, int causal, int window_left, int window_right) {
+                              int max_seqlen_k, int causal, int window_left, int window_right,
+                              int pack_shift) {
   fa::VarlenLaunch L;
   L.sm_count = sm_count;
-  L.item_bound = (long long)num_heads *
-                 (((long long)total_q + (long long)(fa::kRowsPerItem - 1) * batch) /
-                  fa::kRowsPerItem);
+  // With packing an item holds 256 / P tokens of P heads.
+  const long long tpi = fa::kRowsPerItem >> pack_shift;
+  L.item_bound = (long long)(num_heads >> pack_shift) *
+                 (((long long)total_q + (tpi - 1) * batch) / tpi);
   long long kv = total_k;
   if (max_seqlen_k > 0 && max_seqlen_k < kv) kv = max_seqlen_k;
   if (window_left >= 0 && (causal || window_right >= 0)) {
@@ -238,8 +258,6 @@ extern "C" fa_status fa_varlen_fwd_strided(
     int total_q, int total_k, int num_heads, int num_heads_k, int d_qk, int d_v,
     int max_seqlen_q, int max_seqlen_k, float softmax_scale, int causal, int window_left,
     int window_right, void* out, float* lse, fa_stream_t stream) {
-  (void)max_seqlen_q;
-  (void)max_seqlen_k;
   // ---- host validation (before any CUDA call)
   if (!q || !out || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
   if (total_k > 0 && (!k || !v)) return FA_ERR_INVALID_ARG;
@@ -288,13 +306,15 @@ extern "C" fa_status fa_varlen_fwd_strided(
   const long long vrs = total_k > 0 ? v_row_stride : q_row_stride;
   const long long vhs = total_k > 0 ? v_head_stride : q_head_stride;
   const int qt = tail_width(d_qk);
-  bool ok = encode_rows(&maps.q_full, q, d_qk, num_heads, total_q, 64, fa::kBM, q_head_stride,
-                        q_row_stride) &&
+  const int pack_shift = pack_shift_for(batch, total_q, num_heads, num_heads_k, max_seqlen_q);
+  const int qh = 1 << pack_shift;  // heads per Q box, fa::kBM / qh tokens
+  bool ok = encode_rows(&maps.q_full, q, d_qk, num_heads, total_q, 64, fa::kBM / qh,
+                        q_head_stride, q_row_stride, qh) &&
             encode_rows(&maps.k_full, kb, d_qk, kh, tk, 64, fa::kBN, khs, krs) &&
             encode_rows(&maps.v_full, vb, vd, kh, tk, fa::v_atom_width(vd), fa::kBN, vhs, vrs);
   if (ok && qt)
-    ok = encode_rows(&maps.q_tail, q, d_qk, num_heads, total_q, qt, fa::kBM, q_head_stride,
-                     q_row_stride) &&
+    ok = encode_rows(&maps.q_tail, q, d_qk, num_heads, total_q, qt, fa::kBM / qh, q_head_stride,
+                     q_row_stride, qh) &&
          encode_rows(&maps.k_tail, kb, d_qk, kh, tk, qt, fa::kBN, khs, krs);
   if (!ok) return FA_ERR_LAUNCH;
 
@@ -314,18 +334,21 @@ extern "C" fa_status fa_varlen_fwd_strided(
   args.lse = lse;
   args.status = dev->status;
   args.split = 1;
+  args.pack_shift = pack_shift;
 
   const fa::VarlenLaunch L = launch_shape(dev->sm_count, batch, total_q, total_k, num_heads,
-                                          max_seqlen_k, causal, window_left, window_right);
+                                          max_seqlen_k, causal, window_left, window_right,
+                                          pack_shift);
   cudaError_t e = launch(maps, args, L, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 extern "C" fa_status fa_varlen_fwd_plan(int batch, int total_q, int total_k, int num_heads,
-                                        int num_heads_k, int d_qk, int d_v, int max_seqlen_k,
-                                        int causal, int window_left, int window_right,
-                                        int* grid, int* split) {
-  if (!grid || !split) return FA_ERR_INVALID_ARG;
+                                        int num_heads_k, int d_qk, int d_v, int max_seqlen_q,
+                                        int max_seqlen_k, int causal, int window_left,
+                                        int window_right, int* grid, int* split,
+                                        int* heads_per_tile) {
+  if (!grid || !split || !heads_per_tile) return FA_ERR_INVALID_ARG;
   if (batch < 1 || total_q < 0 || total_k < 0 || num_heads < 1 || num_heads_k < 1 ||
       num_heads % num_heads_k != 0 || window_left < -1 || window_right < -1)
     return FA_ERR_INVALID_ARG;
@@ -344,9 +367,12 @@ extern "C" fa_status fa_varlen_fwd_plan(int batch, int total_q, int total_k, int
   if (st != FA_OK) return st;
   *grid = 0;
   *split = 1;
+  const int pack_shift = pack_shift_for(batch, total_q, num_heads, num_heads_k, max_seqlen_q);
+  *heads_per_tile = 1 << pack_shift;
   if (total_q == 0) return FA_OK;
   const fa::VarlenLaunch L = launch_shape(dev->sm_count, batch, total_q, total_k, num_heads,
-                                          max_seqlen_k, causal, window_left, window_right);
+                                          max_seqlen_k, causal, window_left, window_right,
+                                          pack_shift);
   return plan(L, grid, split) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

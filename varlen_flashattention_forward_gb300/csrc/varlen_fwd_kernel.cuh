@@ -192,6 +192,12 @@ struct VarlenArgs {
   // runs part r of the item's KV tiles and the cluster combines the parts
   // (split_combine).
   int split;
+  // GQA head-group packing: P = 1 << pack_shift query heads that share a
+  // key/value head fill one query tile together, row r of a tile being
+  // token r / P and head r % P of the tile's 128 / P tokens (the Q tensor
+  // maps load boxes of {64, P, 128 / P}), so that a K/V tile serves all P
+  // heads at once.  0 = one head per tile.
+  int pack_shift;
 };
 
 struct VarlenMaps {
@@ -339,6 +345,8 @@ struct WorkItem {
   int q_start, k_start, lq, lk, head, kv_head, row0, n_qt, tile_lo, n_kv;
   int b0, nb;  // first sequence of the unit and how many (nb > 1: a pack)
 };
+// Row r of a work item (0 .. 255) is token row0 + (r >> pack_shift) of the
+// sequence and query head head + r % P.
 
 // Short segments: consecutive sequences of 1..kPackMaxLen query rows with as
 // many keys and the same token offsets in Q and K (self-attention over one
@@ -415,8 +423,8 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
 // (The kernel arguments it needs come by value: a reference would make the
 // compiler copy the whole argument block to local memory for the call.)
 static __device__ __noinline__ void build_work_list(const int* cu_q, const int* cu_k, int B,
-                                                    int num_heads, int* s_prefix, int* s_sorted,
-                                                    int* s_part, int* s_tmp) {
+                                                    int num_heads, int pack_shift, int* s_prefix,
+                                                    int* s_sorted, int* s_part, int* s_tmp) {
   const int tid = threadIdx.x;
   int* t_lq = s_tmp;                 // query rows of sequence b
   int* t_key = s_tmp + kMaxBatch;    // sort key of the unit starting at b, -1 for members
@@ -427,15 +435,16 @@ static __device__ __noinline__ void build_work_list(const int* cu_q, const int* 
   for (int b = tid; b < B; b += kVarlenThreads) {
     const int q0 = cu_q[b], k0 = cu_k[b];
     const int lq = cu_q[b + 1] - q0, lk = cu_k[b + 1] - k0;
-    const bool pack = lq >= 1 && lq <= kPackMaxLen && lk == lq && k0 == q0;
+    const bool pack = pack_shift == 0 && lq >= 1 && lq <= kPackMaxLen && lk == lq && k0 == q0;
     s_prefix[b] = pack ? q0 / kPackBlock : -1;
     s_sorted[b] = lk;
     t_lq[b] = lq;
   }
   __syncthreads();
   // 2. Units: a sequence starts one unless it continues its predecessor's
-  //    pack.  Sort key = key rows; the item count (heads x pairs of query
-  //    tiles) goes where the sequence's key count was.
+  //    pack.  Sort key = key rows; the item count (head groups x pairs of
+  //    query tiles) goes where the sequence's key count was.
+  const int tokens_per_item = kRowsPerItem >> pack_shift;
   for (int b = tid; b < B; b += kVarlenThreads) {
     const int blk = s_prefix[b];
     int nb = 0, key = -1;
@@ -445,7 +454,8 @@ static __device__ __noinline__ void build_work_list(const int* cu_q, const int* 
       if (blk >= 0)  // a pack: its members have as many query rows as keys
         for (; b + nb < B && s_prefix[b + nb] == blk; ++nb) key += s_sorted[b + nb];
       const int rows_q = blk >= 0 ? key : t_lq[b];
-      t_lq[b] = num_heads * ((max(rows_q, 0) + kRowsPerItem - 1) / kRowsPerItem);
+      t_lq[b] = (num_heads >> pack_shift) *
+                ((max(rows_q, 0) + tokens_per_item - 1) >> (8 - pack_shift));
     } else {
       t_lq[b] = 0;
     }
@@ -515,7 +525,7 @@ static __device__ __noinline__ void build_work_list(const int* cu_q, const int* 
 
 __device__ __forceinline__ WorkItem decode_item(int it, const VarlenArgs& a,
                                                 const int* s_prefix, const int* s_sorted,
-                                                int split = 1) {
+                                                int split, int pack_shift) {
   // Largest sorted position p with prefix[p] <= it (skips empty sequences).
   int lo = 0, hi = a.batch - 1;
   while (lo < hi) {
@@ -531,13 +541,17 @@ __device__ __forceinline__ WorkItem decode_item(int it, const VarlenArgs& a,
   w.k_start = a.cu_k[w.b0];
   w.lq = a.cu_q[w.b0 + w.nb] - w.q_start;
   w.lk = a.cu_k[w.b0 + w.nb] - w.k_start;
-  const int pairs = (w.lq + kRowsPerItem - 1) / kRowsPerItem;
-  w.head = r / pairs;
-  const int pair = pairs - 1 - (r - w.head * pairs);  // later rows first
+  // An item covers 256 / P tokens of the sequence (1 << tshift) and P heads.
+  static_assert(kRowsPerItem == 256, "tokens per item are 256 >> pack_shift");
+  const int tshift = 8 - pack_shift;
+  const int pairs = (w.lq + (1 << tshift) - 1) >> tshift;
+  const int group = r / pairs;
+  w.head = group << pack_shift;  // first query head of the item
+  const int pair = pairs - 1 - (r - group * pairs);  // later rows first
   w.kv_head = w.head / (a.num_heads / a.num_heads_k);
-  w.row0 = pair * kRowsPerItem;
-  const int row_end = min(w.lq, w.row0 + kRowsPerItem);
-  w.n_qt = (row_end - w.row0 + kBM - 1) / kBM;
+  w.row0 = pair << tshift;  // first token of the item in the sequence
+  const int row_end = min(w.lq, w.row0 + (1 << tshift));
+  w.n_qt = (((row_end - w.row0) << pack_shift) + kBM - 1) / kBM;
   const int off = w.lk - w.lq;
   const int key_lo = a.wl >= 0 ? max(0, w.row0 + off - a.wl) : 0;
   const int key_hi = a.wr >= 0 ? min(w.lk, row_end + off + a.wr) : w.lk;
@@ -596,8 +610,9 @@ static __device__ __noinline__ void split_combine(const VarlenArgs args, uint8_t
   ptx::cluster_arrive_release();
   ptx::cluster_wait_acquire();  // every part is in its CTA's shared memory
   if (it < total_items) {
-    const WorkItem w = decode_item(it, args, s_prefix, s_sorted, S);
-    const int rows = min(kRowsPerItem, w.lq - w.row0);
+    const WorkItem w = decode_item(it, args, s_prefix, s_sorted, S, args.pack_shift);
+    const int rows = min(kRowsPerItem, (w.lq - w.row0) << args.pack_shift);
+    const int pmask = (1 << args.pack_shift) - 1;
     const int r_lo = rows * rank / S, r_hi = rows * (rank + 1) / S;
     const uint32_t base = ptx::smem_u32(smem);
     float* wgt = reinterpret_cast<float*>(smem + St::kWOff);
@@ -620,8 +635,8 @@ static __device__ __noinline__ void split_combine(const VarlenArgs args, uint8_t
       const float inv = L > 0.f ? 1.f / L : 0.f;
       for (int sp = 0; sp < S; ++sp) wr[sp] *= inv;
       if (args.lse) {
-        const size_t tok = (size_t)(w.q_start + w.row0 + r);
-        args.lse[(size_t)w.head * args.total_q + tok] =
+        const size_t tok = (size_t)(w.q_start + w.row0 + (r >> args.pack_shift));
+        args.lse[(size_t)(w.head + (r & pmask)) * args.total_q + tok] =
             L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : neg_inf;
       }
     }
@@ -644,13 +659,14 @@ static __device__ __noinline__ void split_combine(const VarlenArgs args, uint8_t
         acc[0] += ws * v0.x; acc[1] += ws * v0.y; acc[2] += ws * v0.z; acc[3] += ws * v0.w;
         acc[4] += ws * v1.x; acc[5] += ws * v1.y; acc[6] += ws * v1.z; acc[7] += ws * v1.w;
       }
-      const size_t tok = (size_t)(w.q_start + w.row0 + r);
+      const size_t tok = (size_t)(w.q_start + w.row0 + (r >> args.pack_shift));
+      const int head = w.head + (r & pmask);
       uint4 pk;
       pk.x = ptx::pack_bf16x2(acc[0], acc[1]);
       pk.y = ptx::pack_bf16x2(acc[2], acc[3]);
       pk.z = ptx::pack_bf16x2(acc[4], acc[5]);
       pk.w = ptx::pack_bf16x2(acc[6], acc[7]);
-      *reinterpret_cast<uint4*>(args.out + (tok * args.num_heads + w.head) * (size_t)D_V + 8 * g) = pk;
+      *reinterpret_cast<uint4*>(args.out + (tok * args.num_heads + head) * (size_t)D_V + 8 * g) = pk;
     }
   }
   __syncwarp();
@@ -659,14 +675,17 @@ static __device__ __noinline__ void split_combine(const VarlenArgs args, uint8_t
 }
 
 // ------------------------------------------------------------ the kernel
-// kSplit selects the split-KV instantiation (launched in clusters of
-// args.split CTAs); the other one compiles without any split-KV code, whose
-// extra state would otherwise cost the pipeline loops registers.
-template <int D_QK, int D_V, bool kSplit>
+// kGeneral selects the instantiation that runs split-KV (args.split > 1,
+// launched in clusters of args.split CTAs) and GQA head-group packing
+// (args.pack_shift > 0); the other one compiles with neither (split 1,
+// one head per tile as constants): their extra state would otherwise cost
+// the pipeline loops registers.
+template <int D_QK, int D_V, bool kGeneral>
 __global__ void __launch_bounds__(kVarlenThreads, 1)
     varlen_fwd_kernel(const __grid_constant__ VarlenMaps maps, const VarlenArgs args) {
   using C = VarlenCfg<D_QK, D_V>;
-  const int split = kSplit ? args.split : 1;
+  const int split = kGeneral ? args.split : 1;
+  const int pshift = kGeneral ? args.pack_shift : 0;
   using QK = typename C::QK;
   using VD = typename C::VD;
   constexpr int NK = C::nk, NV = C::nv;
@@ -732,7 +751,8 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
   static_assert(SplitStash<D_V>::kBytes <= 2 * C::q_pairs * C::q_tile_bytes +
                                                NK * C::k_slot_bytes + NV * C::v_slot_bytes,
                 "the split-KV partials fit in the Q tiles and K/V rings");
-  build_work_list(args.cu_q, args.cu_k, args.batch, args.num_heads, s_prefix, s_sorted, s_part,
+  build_work_list(args.cu_q, args.cu_k, args.batch, args.num_heads, pshift, s_prefix,
+                  s_sorted, s_part,
                   reinterpret_cast<int*>(k_ring));  // ends with __syncthreads
   ptx::tc_fence_before();
   __syncthreads();
@@ -756,7 +776,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         for (int r = 0; r * (int)gridDim.x < total_items && ok; ++r) {
           const int it = snake_item(r, split);
           if (it >= total_items) continue;
-          const WorkItem w = decode_item(it, args, s_prefix, s_sorted, split);
+          const WorkItem w = decode_item(it, args, s_prefix, s_sorted, split, pshift);
           if (w.n_kv == 0) continue;
           const int pair = C::q_pairs == 2 ? (int)(item_n & 1) : 0;
           ++item_n;
@@ -770,7 +790,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             ptx::mbar_arrive_expect_tx(bar, C::q_tile_bytes);
             qi_par ^= 1u << b;
             qi_any |= 1u << b;
-            const int row = w.q_start + w.row0 + t * kBM;
+            const int row = w.q_start + w.row0 + t * (kBM >> pshift);
             uint8_t* qdst = q_base + b * C::q_tile_bytes;
 #pragma unroll
             for (int c = 0; c < QK::chunks; ++c)
@@ -898,7 +918,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         for (int r = 0; r * (int)gridDim.x < total_items && ok; ++r) {
           const int it = snake_item(r, split);
           if (it >= total_items) continue;
-          const WorkItem w = decode_item(it, args, s_prefix, s_sorted, split);
+          const WorkItem w = decode_item(it, args, s_prefix, s_sorted, split, pshift);
           if (w.n_kv == 0) continue;
           const bool mine = t < w.n_qt;
           const int qb = 2 * (C::q_pairs == 2 ? (int)(item_n & 1) : 0) + t;  // Q buffer
@@ -1026,12 +1046,13 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     for (int r = 0; r * (int)gridDim.x < total_items && ok; ++r) {
       const int it = snake_item(r, split);
       if (it >= total_items) continue;
-      const WorkItem w = decode_item(it, args, s_prefix, s_sorted, split);
+      const WorkItem w = decode_item(it, args, s_prefix, s_sorted, split, pshift);
       const int qb = 2 * (C::q_pairs == 2 ? (int)(item_n & 1) : 0) + t;  // this item's Q buffer
       if (w.n_kv > 0) ++item_n;
       if (t >= w.n_qt) continue;
       release_staged();
-      const int i = w.row0 + t * kBM + row_in_tile;  // query row within the sequence
+      // Query token of this row within the sequence.
+      const int i = w.row0 + ((t * kBM + row_in_tile) >> pshift);
       const bool row_valid = i < w.lq;
       const int off = w.lk - w.lq;
       int lo_i = 0, hi_i = 0;
@@ -1161,7 +1182,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
       }
       if (!ok) break;
 
-      if (kSplit) {
+      if (kGeneral && split > 1) {
         // Split-KV: this CTA holds one part of the item.  Its O stays in
         // TMEM for the cluster combine, and (m, l) go into the row's first
         // two S/P columns, dead once the last P V (before o_full) is done.
@@ -1196,12 +1217,14 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         for (int c = 0; c < C::pv_n; ++c) o[c] = 0u;
       }
       const bool staged = C::stage_o && w.n_kv > 0;
+      // Query head of this row (packed heads: row % P).
+      const int head = w.head + (row_in_tile & ((1 << pshift) - 1));
       uint8_t* const srow = q_base + qb * C::q_tile_bytes + row_in_tile * (D_V * 2);
       if (row_valid) {
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
         const size_t tok = (size_t)(w.q_start + i);
         uint4* dst = reinterpret_cast<uint4*>(args.out +
-                                              (tok * args.num_heads + w.head) * (size_t)D_V);
+                                              (tok * args.num_heads + head) * (size_t)D_V);
         auto pk = [&](int c) {
           return ptx::pack_bf16x2(__uint_as_float(o[c]) * inv_l, __uint_as_float(o[c + 1]) * inv_l);
         };
@@ -1237,20 +1260,20 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         if (args.lse) {
           // Natural-log LSE: (m + log2 l) * ln 2.
           const float lse = l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : neg_inf;
-          args.lse[(size_t)w.head * args.total_q + tok] = lse;
+          args.lse[(size_t)head * args.total_q + tok] = lse;
         }
       }
       if (staged) staged_qb = qb;
     }
     release_staged();
     ptx::bulk_wait_all();  // every O row written before the CTA exits
-    if (kSplit) {
+    if (kGeneral && split > 1) {
       // Both warpgroups are past their last O wait, so every MMA of the item
       // has completed (each issuer's last commit covers all of its MMAs) and
       // the Q tiles and K/V rings are dead: the partial goes there.
       ptx::named_bar_sync_n(1, 256);
       const int it = (int)blockIdx.x / split;
-      const WorkItem w = it < total_items ? decode_item(it, args, s_prefix, s_sorted, split) : WorkItem{};
+      const WorkItem w = it < total_items ? decode_item(it, args, s_prefix, s_sorted, split, pshift) : WorkItem{};
       if (it < total_items && t < w.n_qt) {
         ptx::tc_fence_after();
         const int r = t * kBM + row_in_tile;  // row within the item
@@ -1290,7 +1313,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (kSplit) split_combine<D_V>(args, smem, s_prefix, s_sorted, total_items);
+  if (kGeneral && split > 1) split_combine<D_V>(args, smem, s_prefix, s_sorted, total_items);
   if (warp == kMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
@@ -1415,7 +1438,10 @@ cudaError_t launch_varlen_impl(const VarlenMaps& maps, const VarlenArgs& args_in
   if (args.split == 1) {
     long long grid = L.item_bound < L.sm_count ? L.item_bound : L.sm_count;
     if (grid < 1) grid = 1;
-    varlen_fwd_kernel<D_QK, D_V, false><<<(int)grid, kVarlenThreads, smem, stream>>>(maps, args);
+    if (args.pack_shift == 0)
+      varlen_fwd_kernel<D_QK, D_V, false><<<(int)grid, kVarlenThreads, smem, stream>>>(maps, args);
+    else
+      varlen_fwd_kernel<D_QK, D_V, true><<<(int)grid, kVarlenThreads, smem, stream>>>(maps, args);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg;
