@@ -87,7 +87,10 @@ typedef enum {
  *                 cu[batch] = total_q.  Sequence b owns query tokens
  *                 [cu_seqlens_q[b], cu_seqlens_q[b+1]).
  *   cu_seqlens_k  int32 [batch + 1] device, same for keys/values.
- *   batch         1 .. 1024
+ *   batch         >= 1.  Up to 2048 sequences run as one launch (the
+ *                 kernel sorts their work list in shared memory); a larger
+ *                 batch runs as consecutive launches of up to 2048
+ *                 sequences each, on `stream`.
  *   num_heads, num_heads_k  num_heads % num_heads_k == 0; query head h reads
  *                 key/value head h / (num_heads / num_heads_k).  When the
  *                 query sequences are short (by the max_seqlen_q hint, else
@@ -125,7 +128,7 @@ typedef enum {
  *
  * Host errors: FA_ERR_INVALID_ARG (null required pointer, negative sizes,
  * batch < 1, head counts, window < -1, scale <= 0, unaligned pointers),
- * FA_ERR_UNSUPPORTED (head dims, batch > 1024), FA_ERR_ARCH.
+ * FA_ERR_UNSUPPORTED (head dims), FA_ERR_ARCH.
  */
 fa_status fa_varlen_fwd(const void* q, const void* k, const void* v,
                         const int* cu_seqlens_q, const int* cu_seqlens_k,
@@ -140,14 +143,15 @@ fa_status fa_varlen_fwd(const void* q, const void* k, const void* v,
  * fa_varlen_fwd_strided) would use for a call with these sizes on the
  * current device, without launching anything.  Arguments as fa_varlen_fwd.
  *
- *   *grid   CTAs of the launch (0 when total_q = 0)
+ *   *grid   CTAs of the launch (0 when total_q = 0); with more than 2048
+ *           sequences, of each launch of 2048
  *   *split  CTAs per work item: 1 = persistent grid of at most one CTA per
  *           SM walking the work list; > 1 = split-KV, one cluster of
  *           *split CTAs per work item
  *   *heads_per_tile  query heads packed into one 128-row query tile (GQA
  *           head-group packing): 1, or P in {2, 4, 8, 16}
  *
- * Host errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (head dims, batch),
+ * Host errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (head dims),
  * FA_ERR_ARCH, FA_ERR_LAUNCH (a device query failed).
  */
 fa_status fa_varlen_fwd_plan(int batch, int total_q, int total_k, int num_heads,

@@ -77,7 +77,6 @@ def varlen(lib, **kw):
     (dict(lse=P(0x6002)), fa.FA_ERR_INVALID_ARG),
     (dict(dqk=100, dv=100), fa.FA_ERR_UNSUPPORTED),
     (dict(dqk=192, dv=192), fa.FA_ERR_UNSUPPORTED),
-    (dict(batch=1025), fa.FA_ERR_UNSUPPORTED),
 ])
 def test_varlen_host_validation(lib, kw, expect):
     assert varlen(lib, **kw) == expect

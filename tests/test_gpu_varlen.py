@@ -211,10 +211,38 @@ def test_bitwise_deterministic(cuda_device):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def test_max_batch(cuda_device):
-    lens = [(i * 37) % 130 for i in range(1024)]
+def test_max_batch_one_launch(cuda_device):
+    # 2048 sequences: the largest batch one launch sorts in shared memory.
+    lens = [(i * 37) % 130 for i in range(2048)]
     q, k, v, cq, ck = make(lens, lens, 1, 1, 64, 64, seed=15)
     compare(q, k, v, cq, ck, 0.125)
+
+
+def test_batch_beyond_one_launch(cuda_device):
+    # 5000 sequences (zero-length ones among them) run as three launches of
+    # at most 2048 sequences; q shorter than k in some, so that causal rows
+    # see keys from the bottom-right.
+    rng = torch.Generator().manual_seed(29)
+    lens_q = torch.randint(0, 40, (5000,), generator=rng).tolist()
+    lens_k = [lq + int(x) for lq, x in zip(lens_q, torch.randint(0, 3, (5000,), generator=rng))]
+    q, k, v, cq, ck = make(lens_q, lens_k, 2, 1, 64, 64, seed=30)
+    compare(q, k, v, cq, ck, 0.125, causal=True)
+    a = run_gpu(q, k, v, cq, ck, 0.125, causal=True)
+    b = run_gpu(q, k, v, cq, ck, 0.125, causal=True)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_many_windows_and_long_images(cuda_device):
+    # Two 4K-image layers' worth of 64-token windows (2 x 700 segments, the
+    # windowed layers of the sglang FA4 PR, "Speed Tests and Profiling") next
+    # to two full images: 1402 segments in one launch, windows packed.
+    lens = [64] * 700 + [4096] + [64] * 700 + [2000]
+    q, k, v, cq, ck = make(lens, lens, 4, 4, 80, 80, seed=31, std=0.5)
+    rows = sample_rows(lens, 4, 3000, seed=31)
+    out, lse = run_gpu(q, k, v, cq, ck, 80 ** -0.5)
+    compare(q, k, v, cq, ck, 80 ** -0.5, rows=rows, out=out, lse=lse)
+    out2, lse2 = run_gpu(q, k, v, cq, ck, 80 ** -0.5)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
 
 
 # ------------------------------------------------------------ full sizes

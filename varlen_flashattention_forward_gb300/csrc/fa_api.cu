@@ -269,7 +269,6 @@ extern "C" fa_status fa_varlen_fwd_strided(
   if (!aligned(q, 16) || !aligned(out, 16) || (k && !aligned(k, 16)) || (v && !aligned(v, 16)) ||
       !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4) || (lse && !aligned(lse, 4)))
     return FA_ERR_INVALID_ARG;
-  if (batch > fa::kMaxBatch) return FA_ERR_UNSUPPORTED;
   typedef cudaError_t (*Launcher)(const fa::VarlenMaps&, const fa::VarlenArgs&,
                                   const fa::VarlenLaunch&, cudaStream_t);
   Launcher launch = nullptr;
@@ -319,9 +318,6 @@ extern "C" fa_status fa_varlen_fwd_strided(
   if (!ok) return FA_ERR_LAUNCH;
 
   fa::VarlenArgs args;
-  args.cu_q = cu_seqlens_q;
-  args.cu_k = cu_seqlens_k;
-  args.batch = batch;
   args.num_heads = num_heads;
   args.num_heads_k = num_heads_k;
   args.total_q = total_q;
@@ -336,11 +332,22 @@ extern "C" fa_status fa_varlen_fwd_strided(
   args.split = 1;
   args.pack_shift = pack_shift;
 
-  const fa::VarlenLaunch L = launch_shape(dev->sm_count, batch, total_q, total_k, num_heads,
-                                          max_seqlen_k, causal, window_left, window_right,
-                                          pack_shift);
-  cudaError_t e = launch(maps, args, L, reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  // One launch per chunk of at most kMaxBatch sequences (the kernel keeps a
+  // chunk's work list in shared memory).  cu_seqlens hold absolute token
+  // offsets, so a chunk is the same arrays from its first sequence on; the
+  // chunks' outputs and LSE rows are disjoint.
+  for (long long b0 = 0; b0 < batch; b0 += fa::kMaxBatch) {
+    const int nb = (int)std::min<long long>(fa::kMaxBatch, batch - b0);
+    args.cu_q = cu_seqlens_q + b0;
+    args.cu_k = cu_seqlens_k + b0;
+    args.batch = nb;
+    const fa::VarlenLaunch L = launch_shape(dev->sm_count, nb, total_q, total_k, num_heads,
+                                            max_seqlen_k, causal, window_left, window_right,
+                                            pack_shift);
+    const cudaError_t e = launch(maps, args, L, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
 }
 
 extern "C" fa_status fa_varlen_fwd_plan(int batch, int total_q, int total_k, int num_heads,
@@ -352,7 +359,6 @@ extern "C" fa_status fa_varlen_fwd_plan(int batch, int total_q, int total_k, int
   if (batch < 1 || total_q < 0 || total_k < 0 || num_heads < 1 || num_heads_k < 1 ||
       num_heads % num_heads_k != 0 || window_left < -1 || window_right < -1)
     return FA_ERR_INVALID_ARG;
-  if (batch > fa::kMaxBatch) return FA_ERR_UNSUPPORTED;
   typedef cudaError_t (*Planner)(const fa::VarlenLaunch&, int*, int*);
   Planner plan = nullptr;
   if (d_qk == 64 && d_v == 64) plan = fa::plan_varlen_64_64;
@@ -370,9 +376,9 @@ extern "C" fa_status fa_varlen_fwd_plan(int batch, int total_q, int total_k, int
   const int pack_shift = pack_shift_for(batch, total_q, num_heads, num_heads_k, max_seqlen_q);
   *heads_per_tile = 1 << pack_shift;
   if (total_q == 0) return FA_OK;
-  const fa::VarlenLaunch L = launch_shape(dev->sm_count, batch, total_q, total_k, num_heads,
-                                          max_seqlen_k, causal, window_left, window_right,
-                                          pack_shift);
+  const fa::VarlenLaunch L =
+      launch_shape(dev->sm_count, std::min(batch, fa::kMaxBatch), total_q, total_k, num_heads,
+                   max_seqlen_k, causal, window_left, window_right, pack_shift);
   return plan(L, grid, split) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

@@ -68,7 +68,7 @@ constexpr uint32_t kControlRegs = 64;
 constexpr int kBM = 128;              // query rows per tile
 constexpr int kBN = 128;              // keys per KV tile
 constexpr int kRowsPerItem = 2 * kBM; // two query tiles per work item
-constexpr int kMaxBatch = 1024;
+constexpr int kMaxBatch = 2048;       // sequences per launch (larger batches: several launches)
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold, log2 units
 constexpr int kSmemBudget = 232448;   // 227 KB opt-in per CTA
 constexpr int kBarrierBytes = 448;    // VarlenBarriers, reserved in the smem budget
@@ -412,11 +412,10 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
 }
 
 // ------------------------------------------------------------ work list
-// Builds, in shared memory, the sequences sorted by key length (longest
-// first, ties by index) and the prefix sum of their work-item counts.
-// The key array doubles as the prefix array once the ranks are known.
-// Builds the sorted unit list and the item prefix sums in shared memory.
-// s_tmp: 3 * kMaxBatch ints of scratch (the K ring, empty until the producer
+// Builds, in shared memory, the work units (sequences, or packs of short
+// segments) sorted by key length (longest first, ties by index) and the
+// prefix sum of their work-item counts.
+// s_tmp: 5 * kMaxBatch ints of scratch (the K ring, empty until the producer
 // starts), so that nothing is held in registers across the barriers.  Kept
 // out of line: it runs once per CTA, and inlined it changed the register
 // allocation of the pipeline loops (ViT d80 1.5 % slower).
@@ -429,6 +428,7 @@ static __device__ __noinline__ void build_work_list(const int* cu_q, const int* 
   int* t_lq = s_tmp;                 // query rows of sequence b
   int* t_key = s_tmp + kMaxBatch;    // sort key of the unit starting at b, -1 for members
   int* t_unit = s_tmp + 2 * kMaxBatch;  // nb of the unit starting at b (0 for members)
+  uint64_t* t_sort = reinterpret_cast<uint64_t*>(s_tmp + 3 * kMaxBatch);  // sort keys
   // 1. The only global reads: s_prefix[b] = the kPackBlock-token block of a
   //    packable sequence's first token (-1 for any other sequence),
   //    s_sorted[b] = its key count.
@@ -463,18 +463,37 @@ static __device__ __noinline__ void build_work_list(const int* cu_q, const int* 
     t_unit[b] = nb;
   }
   __syncthreads();
-  // 3. Longest first: the rank of every entry by key (members last, ties in
-  //    sequence order); s_sorted[rank] = b | nb << kUnitShift and
-  //    s_prefix[rank] = its item count.
-  for (int b = tid; b < B; b += kVarlenThreads) {
-    const int kb = t_key[b];
-    int rank = 0;
-    for (int o = 0; o < B; ++o) {
-      const int ko = t_key[o];
-      rank += (ko > kb) || (ko == kb && o < b);
+  // 3. Longest first: the entries sorted by key, descending (ties in
+  //    sequence order, members last), with a bitonic network over N = B
+  //    rounded up to a power of two (padding entries sort after everything);
+  //    then s_sorted[rank] = b | nb << kUnitShift and s_prefix[rank] = its
+  //    item count.  Every CTA sorts the same keys the same way, so all agree
+  //    on the order.
+  int n_sort = 1;
+  while (n_sort < B) n_sort <<= 1;
+  for (int b = tid; b < n_sort; b += kVarlenThreads)
+    t_sort[b] = b < B ? ((uint64_t)(uint32_t)(t_key[b] + 1) << 32) | (uint32_t)(0xffffffffu - b)
+                      : 0ull;
+  __syncthreads();
+  for (int k = 2; k <= n_sort; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < n_sort / 2; i += kVarlenThreads) {
+        const int lo = 2 * i - (i & (j - 1));  // the i-th pair (lo, lo + j)
+        const uint64_t x = t_sort[lo], y = t_sort[lo + j];
+        // Blocks of k entries alternate direction; the last merge is
+        // descending.
+        if (((lo & k) == 0) == (x < y)) {
+          t_sort[lo] = y;
+          t_sort[lo + j] = x;
+        }
+      }
+      __syncthreads();
     }
-    s_sorted[rank] = b | (t_unit[b] << kUnitShift);
-    s_prefix[rank] = t_lq[b];
+  }
+  for (int r = tid; r < B; r += kVarlenThreads) {
+    const int b = (int)(0xffffffffu - (uint32_t)t_sort[r]);
+    s_sorted[r] = b | (t_unit[b] << kUnitShift);
+    s_prefix[r] = t_lq[b];
   }
   __syncthreads();
   // Block-wide exclusive scan of per-unit item counts in sorted order.
@@ -746,7 +765,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     ptx::tmem_alloc(ptx::smem_u32(&cb->tmem_base), 512);
     ptx::tmem_relinquish();
   }
-  static_assert(NK * C::k_slot_bytes >= 3 * kMaxBatch * (int)sizeof(int),
+  static_assert(NK * C::k_slot_bytes >= 5 * kMaxBatch * (int)sizeof(int),
                 "the K ring holds the work-list scratch");
   static_assert(SplitStash<D_V>::kBytes <= 2 * C::q_pairs * C::q_tile_bytes +
                                                NK * C::k_slot_bytes + NV * C::v_slot_bytes,

@@ -274,9 +274,29 @@ def gqa_decode_like(group: int = 8) -> VarlenWorkload:
                           128, 128, 128 ** -0.5, causal=True, seed=9)
 
 
+def vit_many_windows(d: int = 80) -> VarlenWorkload:
+    """Two 4K-image windowed layers' worth of 64-token windows (700 each, the
+    Qwen2.5-VL windowed layers of the sglang FA4 PR, "Speed Tests and
+    Profiling") next to two full images of 4096 and 2000 tokens: 1402
+    segments in one call, 16 heads."""
+    lens = [64] * 700 + [4096] + [64] * 700 + [2000]
+    return VarlenWorkload(f"vit_many_windows_d{d}", lens, list(lens), 16, 16, d, d, d ** -0.5,
+                          qk_std=0.5, seed=10, return_lse=False)
+
+
+def work_list_2048() -> VarlenWorkload:
+    """2048 one-token sequences, one head: almost no attention work, so the
+    time is the work-list build (sort and scan of 2048 sequences in every
+    CTA) plus launch overhead."""
+    return VarlenWorkload("work_list_2048", [1] * 2048, [1] * 2048, 1, 1, 64, 64, 0.125,
+                          seed=11, return_lse=False)
+
+
 # Workloads timed only in the bench's extra block (and covered by parity
 # tests at reduced sizes).
 EXTRA_ONLY = {
+    "vit_many_windows_d80": lambda: vit_many_windows(80),
+    "work_list_2048": work_list_2048,
     "splitkv_q256_k65536": splitkv_long_k,
     "splitkv_q1x8_k32768_mla": splitkv_decode_like,
     "gqa4_causal_4x4096": lambda: gqa_prefill(4),
