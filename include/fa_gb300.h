@@ -320,6 +320,22 @@ fa_status fa_merge_attn_states(void* out, float* out_lse, const void* prefix_out
  */
 fa_status fa_get_device_status(void);
 
+/*
+ * fa_set_wait_limit_ns -- sets the time limit of the kernels' pipeline
+ * waits for every later launch of the library in this process (all
+ * devices); 0 restores the default of 4 s.  The method's pages have no
+ * counterpart: it is a diagnostic and test hook.  Every wait inside the
+ * kernels is bounded; when one runs out, the kernel records
+ * FA_ERR_DEVICE_TIMEOUT in the device status word, the other warps of its
+ * CTA give up their waits too, and the CTA lets the copies and tensor-core
+ * operations it started complete, frees its tensor memory and exits (the
+ * outputs of that call are undefined).  Normal waits last microseconds; a
+ * limit of a few microseconds makes a long call run out on purpose, which
+ * exercises that path without any fault.  Limits below 1 ms poll the
+ * barriers without suspending the thread.  Always FA_OK.
+ */
+fa_status fa_set_wait_limit_ns(unsigned long long ns);
+
 /* Human-readable name of a status code (static string). */
 const char* fa_status_string(fa_status s);
 

@@ -22,6 +22,7 @@ Entry points (same names as the C ABI):
   fa_merge_attn_states(prefix_out, prefix_lse, suffix_out, suffix_lse,
                        out=None, out_lse=None, stream=None)
   fa_get_device_status()
+  fa_set_wait_limit_ns(ns)
 """
 from __future__ import annotations
 
@@ -43,7 +44,7 @@ LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
 # Exported C symbols (kept in sync with include/fa_gb300.h; a CPU test checks).
 EXPORTS = ("fa_varlen_fwd", "fa_varlen_fwd_plan", "fa_varlen_fwd_strided", "fa_sparse_mla_decode",
            "fa_sparse_mla_decode_plan", "fa_sparse_mla_decode_noalloc", "fa_merge_attn_states",
-           "fa_get_device_status", "fa_status_string")
+           "fa_get_device_status", "fa_set_wait_limit_ns", "fa_status_string")
 
 _lib = None
 
@@ -88,6 +89,8 @@ def load_library():
     lib.fa_sparse_mla_decode_noalloc.restype = i32
     lib.fa_merge_attn_states.argtypes = [p, p, p, p, p, p, i32, i32, i32, p]
     lib.fa_merge_attn_states.restype = i32
+    lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    lib.fa_set_wait_limit_ns.restype = i32
     lib.fa_get_device_status.argtypes = []
     lib.fa_get_device_status.restype = i32
     lib.fa_status_string.argtypes = [i32]
@@ -310,6 +313,13 @@ def fa_merge_attn_states(prefix_out, prefix_lse, suffix_out, suffix_lse, out=Non
     if st != FA_OK:
         raise FaError(st, "fa_merge_attn_states")
     return out, out_lse
+
+
+def fa_set_wait_limit_ns(ns: int) -> None:
+    """Time limit of the kernels' pipeline waits for later launches (0 = the
+    default of 4 s); a test hook, see fa_set_wait_limit_ns in
+    include/fa_gb300.h."""
+    load_library().fa_set_wait_limit_ns(int(ns))
 
 
 def fa_get_device_status() -> int:

@@ -10,6 +10,7 @@
 // more than the stream's buffer holds allocates a larger one and keeps the
 // old one allocated (a CUDA graph captured earlier may still point at it).
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -63,6 +64,9 @@ struct DeviceInfo {
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
+
+// Time limit of the kernels' pipeline waits, passed to every launch.
+std::atomic<unsigned long long> g_wait_limit_ns{fa::kWaitLimitNs};
 
 // Per-device facts, queried once.  The first call on a device therefore
 // performs runtime queries (no stream work); make it before any stream
@@ -331,6 +335,7 @@ extern "C" fa_status fa_varlen_fwd_strided(
   args.status = dev->status;
   args.split = 1;
   args.pack_shift = pack_shift;
+  args.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
 
   // One launch per chunk of at most kMaxBatch sequences (the kernel keeps a
   // chunk's work list in shared memory).  cu_seqlens hold absolute token
@@ -505,6 +510,7 @@ fa_status plan_decode(const void* q, const void* kv_cache, const int* page_table
   a.range_r = (int)(granules % sp.grid);
   a.part_o = nullptr;
   a.part_lse = nullptr;
+  a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   if (plan->split) {
     plan->o_bytes = (size_t)2 * sp.grid * 64 * fa::kDv * sizeof(float);
     plan->l_bytes = (size_t)2 * sp.grid * 64 * sizeof(float);
@@ -630,6 +636,11 @@ extern "C" fa_status fa_get_device_status(void) {
   const unsigned int zero = 0;
   if (cudaMemcpyToSymbol(g_fa_status, &zero, sizeof zero) != cudaSuccess) return FA_ERR_LAUNCH;
   return (v & fa::kStatusTimeout) ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+}
+
+extern "C" fa_status fa_set_wait_limit_ns(unsigned long long ns) {
+  g_wait_limit_ns.store(ns == 0 ? fa::kWaitLimitNs : ns, std::memory_order_relaxed);
+  return FA_OK;
 }
 
 extern "C" const char* fa_status_string(fa_status s) {

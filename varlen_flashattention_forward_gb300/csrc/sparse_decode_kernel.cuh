@@ -99,6 +99,7 @@ struct DecodeArgs {
   int gran, range_q, range_r;
   float* part_o;          // [2 * grid][64][512] O/l of partial segments (NULL: none)
   float* part_lse;        // [2 * grid][64] their natural-log LSE
+  uint64_t wait_limit_ns; // pipeline wait limit (bounded waits)
 };
 
 // First tile of CTA b's range: the first range_r CTAs take range_q + 1
@@ -342,7 +343,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       for (int c = 0; c < kChunks; ++c) {
         if (i >= 2 && (c == 0 || (c < 8 && release_group(c) != release_group(c - 1)))) {
           ok = wait_warp(ptx::smem_u32(&cb->r_free[st][release_group(c)]), ((i >> 1) - 1) & 1,
-                         abort_flag, a.status);
+                         abort_flag, a.status, a.wait_limit_ns);
           if (!ok) break;
         }
 #pragma unroll
@@ -367,6 +368,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       const uint64_t qd = ptx::smem_desc(ptx::smem_u32(q_s), 16, 1024, ptx::kLayoutSw128);
       bool ok = true;
       int seg = 0;
+      bool q_inflight = true;  // Q load number seg issued, its wait not yet passed
       for (int i = 0; i < n && ok; ++i) {
         const int st = i & 1;
         if (seg_first(i)) {
@@ -374,7 +376,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             // Every S MMA that reads the current Q must be done before the
             // next segment's Q replaces it.
             ptx::mma_commit_elect(ptx::smem_u32(&cb->q_free));
-            ok = wait_warp(ptx::smem_u32(&cb->q_free), (seg - 1) & 1, abort_flag, a.status);
+            ok = wait_warp(ptx::smem_u32(&cb->q_free), (seg - 1) & 1, abort_flag, a.status, a.wait_limit_ns);
             if (!ok) break;
             // (Segment 0's Q was issued at kernel start.)
             if (lane == 0) {
@@ -387,20 +389,22 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                                  ptx::smem_u32(&cb->q_full), c * 64, head0, token);
             }
             __syncwarp();
+            q_inflight = true;
           }
-          ok = wait_warp(ptx::smem_u32(&cb->q_full), seg & 1, abort_flag, a.status);
+          ok = wait_warp(ptx::smem_u32(&cb->q_full), seg & 1, abort_flag, a.status, a.wait_limit_ns);
           if (!ok) break;
+          q_inflight = false;
           ++seg;
         }
         if (i >= 2) {
           ok = wait_warp(ptx::smem_u32(&cb->s_free[st]), ((i >> 1) - 1) & 1, abort_flag,
-                         a.status);
+                         a.status, a.wait_limit_ns);
           if (!ok) break;
         }
         const uint64_t rd = ptx::smem_desc(ptx::smem_u32(stage[st]), 16, 1024, ptx::kLayoutSw128);
         const uint32_t d = tmem + (uint32_t)(st * NP);
         for (int c = 0; c < kChunks && ok; ++c) {
-          ok = wait_warp(ptx::smem_u32(&cb->r_full[st][c]), (i >> 1) & 1, abort_flag, a.status);
+          ok = wait_warp(ptx::smem_u32(&cb->r_full[st][c]), (i >> 1) & 1, abort_flag, a.status, a.wait_limit_ns);
           if (!ok) break;
           // The gathered rows were written by cp.async (generic proxy); order
           // them before the tensor core's (async proxy) reads.
@@ -414,7 +418,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         ptx::mma_commit_elect(ptx::smem_u32(&cb->s_full[st]));
       }
       ptx::mma_commit_elect(ptx::smem_u32(&cb->drain));
-      wait_warp(ptx::smem_u32(&cb->drain), 0, abort_flag, a.status);
+      wait_drain_warp(ptx::smem_u32(&cb->drain), 0, a.status);
+      // A Q reload still in flight (the wait for it gave up) lands before
+      // the CTA exits.
+      if (q_inflight) wait_drain_warp(ptx::smem_u32(&cb->q_full), seg & 1, a.status);
     } else if (warp == 9) {
       // Oᵀ += R(i)[:, 0:512]ᵀ Pᵀ(i), one 128-column m-tile at a time; each
       // m-tile's commit releases the chunks it was the last to read.  The
@@ -424,12 +431,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       int seg = 0;
       for (int i = 0; i < n && ok; ++i) {
         const int st = i & 1;
-        ok = wait_warp(ptx::smem_u32(&cb->p_full[st]), (i >> 1) & 1, abort_flag, a.status);
+        ok = wait_warp(ptx::smem_u32(&cb->p_full[st]), (i >> 1) & 1, abort_flag, a.status, a.wait_limit_ns);
         if (!ok) break;
         const bool first = seg_first(i);
         if (first) {
           if (seg > 0) {
-            ok = wait_warp(ptx::smem_u32(&cb->o_free), (seg - 1) & 1, abort_flag, a.status);
+            ok = wait_warp(ptx::smem_u32(&cb->o_free), (seg - 1) & 1, abort_flag, a.status, a.wait_limit_ns);
             if (!ok) break;
           }
           ++seg;
@@ -454,7 +461,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         ptx::mma_commit_elect(ptx::smem_u32(&cb->pv_done[st]));
       }
       ptx::mma_commit_elect(ptx::smem_u32(&cb->drain));
-      wait_warp(ptx::smem_u32(&cb->drain), 0, abort_flag, a.status);
+      wait_drain_warp(ptx::smem_u32(&cb->drain), 0, a.status);
     }
   } else {
     ptx::regs_inc<kDecodeSoftmaxRegs>();
@@ -482,7 +489,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const bool first = i == seg_start;
         // Every wait is followed by a warpgroup-wide agreement, so that no warp
         // can be left alone at a later named barrier after another gave up.
-        ok = wait_warp(ptx::smem_u32(&cb->s_full[st]), (i >> 1) & 1, abort_flag, a.status);
+        ok = wait_warp(ptx::smem_u32(&cb->s_full[st]), (i >> 1) & 1, abort_flag, a.status, a.wait_limit_ns);
         ok = named_bar_and(3, 128, ok);
         if (!ok) break;
         ptx::tc_fence_after();
@@ -532,7 +539,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             // Oᵀ holds the segment's earlier tiles: wait for the last PV, then
             // scale every head column by its factor.
             ok = wait_warp(ptx::smem_u32(&cb->pv_done[(i - 1) & 1]), ((i - 1) >> 1) & 1,
-                           abort_flag, a.status);
+                           abort_flag, a.status, a.wait_limit_ns);
             ok = named_bar_and(3, 128, ok);
             if (!ok) break;
             ptx::tc_fence_after();
@@ -618,7 +625,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       // A commit tracks every earlier MMA of its issuer, so PV(i) done means
       // all of the segment's Oᵀ is final.
       ok = wait_warp(ptx::smem_u32(&cb->pv_done[seg_end & 1]), (seg_end >> 1) & 1, abort_flag,
-                     a.status);
+                     a.status, a.wait_limit_ns);
       ok = named_bar_and(3, 128, ok);
       if (!ok) break;
       ptx::tc_fence_after();

@@ -198,6 +198,7 @@ struct VarlenArgs {
   // maps load boxes of {64, P, 128 / P}), so that a K/V tile serves all P
   // heads at once.  0 = one head per tile.
   int pack_shift;
+  uint64_t wait_limit_ns;  // pipeline wait limit (bounded waits)
 };
 
 struct VarlenMaps {
@@ -364,20 +365,40 @@ constexpr int kUnitShift = 16;
 static_assert(kMaxBatch < (1 << kUnitShift), "unit encoding");
 
 // ------------------------------------------------------------ bounded waits
-// Wait time limit for any pipeline barrier.  Normal waits are microseconds;
-// hitting the limit means the pipeline is broken.  The kernel then records
-// kStatusTimeout, raises the CTA abort flag and unwinds instead of hanging.
+// Time limit of the pipeline barrier waits, passed per launch (default
+// kWaitLimitNs; fa_set_wait_limit_ns changes it).  Normal waits are
+// microseconds; hitting the limit means the pipeline is broken.  The kernel
+// then records kStatusTimeout, raises the CTA abort flag and unwinds instead
+// of hanging.  Limits below kShortWaitNs (a test setting) poll with the
+// non-blocking probe and read the clock on every poll, so that a wait longer
+// than the limit always runs out.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
+constexpr uint64_t kShortWaitNs = 1000000ull;
+// Limit of the unwind's own waits (for the copies and MMAs a CTA started),
+// which do not give up on the abort flag.
+constexpr uint64_t kDrainLimitNs = 4000000000ull;
 
 __device__ __forceinline__ bool wait_single(uint32_t bar, uint32_t parity,
-                                            volatile int* abort_flag, unsigned int* status) {
+                                            volatile int* abort_flag, unsigned int* status,
+                                            uint64_t limit_ns) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
+  if (limit_ns < kShortWaitNs) {
+    for (;;) {
+      if (ptx::mbar_test_wait(bar, parity)) return true;
+      if (*abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > limit_ns) {
+        atomicOr(status, kStatusTimeout);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
   for (uint32_t spin = 1;; ++spin) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if ((spin & 255u) == 0) {
       if (*abort_flag) return false;
-      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (ptx::globaltimer_ns() - t0 > limit_ns) {
         atomicOr(status, kStatusTimeout);
         *abort_flag = 1;
         return false;
@@ -389,7 +410,48 @@ __device__ __forceinline__ bool wait_single(uint32_t bar, uint32_t parity,
 // Warp-uniform variant: every lane of the warp gets the same answer, so the
 // warp stays converged for the warp-collective tcgen05 loads and stores.
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
-                                          volatile int* abort_flag, unsigned int* status) {
+                                          volatile int* abort_flag, unsigned int* status,
+                                          uint64_t limit_ns) {
+  const unsigned full = 0xffffffffu;
+  if (__all_sync(full, ptx::mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  const bool short_limit = limit_ns < kShortWaitNs;
+  for (uint32_t spin = 1;; ++spin) {
+    const bool done = short_limit ? ptx::mbar_test_wait(bar, parity) : ptx::mbar_try_wait(bar, parity);
+    if (__all_sync(full, done)) return true;
+    if (short_limit || (spin & 255u) == 0) {
+      int give_up = 0;
+      if ((threadIdx.x & 31) == 0) {
+        if (*abort_flag) {
+          give_up = 1;
+        } else if (ptx::globaltimer_ns() - t0 > limit_ns) {
+          atomicOr(status, kStatusTimeout);
+          *abort_flag = 1;
+          give_up = 1;
+        }
+      }
+      if (__shfl_sync(full, give_up, 0)) return false;
+    }
+  }
+}
+
+// The unwind's waits: for copies and MMAs this CTA started, which complete
+// whatever the rest of the pipeline does, so they ignore the abort flag;
+// bounded all the same.
+__device__ __forceinline__ bool wait_drain_single(uint32_t bar, uint32_t parity,
+                                                  unsigned int* status) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t spin = 1;; ++spin) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((spin & 255u) == 0 && ptx::globaltimer_ns() - t0 > kDrainLimitNs) {
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ bool wait_drain_warp(uint32_t bar, uint32_t parity,
+                                                unsigned int* status) {
   const unsigned full = 0xffffffffu;
   if (__all_sync(full, ptx::mbar_try_wait(bar, parity))) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
@@ -397,14 +459,9 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
     if (__all_sync(full, ptx::mbar_try_wait(bar, parity))) return true;
     if ((spin & 255u) == 0) {
       int give_up = 0;
-      if ((threadIdx.x & 31) == 0) {
-        if (*abort_flag) {
-          give_up = 1;
-        } else if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
-          atomicOr(status, kStatusTimeout);
-          *abort_flag = 1;
-          give_up = 1;
-        }
+      if ((threadIdx.x & 31) == 0 && ptx::globaltimer_ns() - t0 > kDrainLimitNs) {
+        atomicOr(status, kStatusTimeout);
+        give_up = 1;
       }
       if (__shfl_sync(full, give_up, 0)) return false;
     }
@@ -802,7 +859,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           for (int t = 0; t < w.n_qt && ok; ++t) {
             const int b = 2 * pair + t;
             ok = wait_single(ptx::smem_u32(&cb->q_free[b]), ((qf_par >> b) & 1) ^ 1, abort_flag,
-                             args.status);
+                             args.status, args.wait_limit_ns);
             qf_par ^= 1u << b;
             if (!ok) break;
             const uint32_t bar = ptx::smem_u32(&cb->q_full[b]);
@@ -822,7 +879,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             // K_j into the K ring.
             const uint32_t ks = ring_slot<NK>(kn);
             ok = wait_single(ptx::smem_u32(&cb->k_free[ks]), ((kn / NK) & 1) ^ 1, abort_flag,
-                             args.status);
+                             args.status, args.wait_limit_ns);
             if (!ok) break;
             {
               const uint32_t bar = ptx::smem_u32(&cb->k_full[ks]);
@@ -838,7 +895,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             // V_j into the V ring.
             const uint32_t vs = ring_slot<NV>(vn);
             ok = wait_single(ptx::smem_u32(&cb->v_free[vs]), ((vn / NV) & 1) ^ 1, abort_flag,
-                             args.status);
+                             args.status, args.wait_limit_ns);
             if (!ok) break;
             {
               const uint32_t bar = ptx::smem_u32(&cb->v_full[vs]);
@@ -856,15 +913,15 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           // Let every copy this thread started land before the CTA exits.
           for (int b = 0; b < 4; ++b)
             if ((qi_any >> b) & 1)
-              wait_single(ptx::smem_u32(&cb->q_full[b]), ((qi_par >> b) & 1) ^ 1, abort_flag,
-                          args.status);
+              wait_drain_single(ptx::smem_u32(&cb->q_full[b]), ((qi_par >> b) & 1) ^ 1,
+                                args.status);
           // Slot s was last filled by tile s + size * ((n - 1 - s) / size).
           for (uint32_t s = 0; s < (uint32_t)NK && s < kn; ++s)
-            wait_single(ptx::smem_u32(&cb->k_full[s]), ((kn - 1 - s) / NK) & 1, abort_flag,
-                        args.status);
+            wait_drain_single(ptx::smem_u32(&cb->k_full[s]), ((kn - 1 - s) / NK) & 1,
+                              args.status);
           for (uint32_t s = 0; s < (uint32_t)NV && s < vn; ++s)
-            wait_single(ptx::smem_u32(&cb->v_full[s]), ((vn - 1 - s) / NV) & 1, abort_flag,
-                        args.status);
+            wait_drain_single(ptx::smem_u32(&cb->v_full[s]), ((vn - 1 - s) / NV) & 1,
+                              args.status);
         }
       }
       __syncwarp();
@@ -883,7 +940,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         auto take_turn = [&]() -> bool {
           if (!C::turns || (t == 0 && groups == 0)) return true;
           const uint32_t par = (t == 0 ? groups - 1 : groups) & 1;
-          return wait_warp(ptx::smem_u32(&cb->turn[t]), par, abort_flag, args.status);
+          return wait_warp(ptx::smem_u32(&cb->turn[t]), par, abort_flag, args.status, args.wait_limit_ns);
         };
         auto pass_turn = [&]() {
           if (C::turns) ptx::mbar_arrive_elect(ptx::smem_u32(&cb->turn[t ^ 1]));
@@ -944,7 +1001,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           ++item_n;
           if (mine) {
             ok = wait_warp(ptx::smem_u32(&cb->q_full[qb]), (q_par >> qb) & 1, abort_flag,
-                           args.status);
+                           args.status, args.wait_limit_ns);
             q_par ^= 1u << qb;
             if (!ok) break;
             set_q(qb);
@@ -953,7 +1010,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           {
             const uint32_t ks = ring_slot<NK>(kn);
             ok = wait_warp(ptx::smem_u32(&cb->k_full[ks]), (kn / NK) & 1, abort_flag,
-                           args.status);
+                           args.status, args.wait_limit_ns);
             if (ok) ok = take_turn();
             if (!ok) break;
             ptx::tc_fence_after();
@@ -976,13 +1033,13 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             constexpr bool kEarlyK = NK > 1;
             const uint32_t vs = ring_slot<NV>(vn);
             ok = wait_warp(ptx::smem_u32(&cb->v_full[vs]), (vn / NV) & 1, abort_flag,
-                           args.status);
+                           args.status, args.wait_limit_ns);
             if (!ok) break;
             ++vn;
             const uint32_t ks = ring_slot<NK>(kn);
             auto wait_k = [&]() -> bool {
               const bool r = wait_warp(ptx::smem_u32(&cb->k_full[ks]), (kn / NK) & 1, abort_flag,
-                                       args.status);
+                                       args.status, args.wait_limit_ns);
               ++kn;
               return r;
             };
@@ -995,17 +1052,17 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             if (mine) {
               if (j == 0) {
                 ok = wait_warp(ptx::smem_u32(&cb->o_free[t]), (ofn & 1) ^ 1, abort_flag,
-                               args.status);
+                               args.status, args.wait_limit_ns);
                 ++ofn;
                 if (!ok) break;
               }
               if (C::split_pv) {
-                ok = wait_warp(ptx::smem_u32(&cb->p_half[t]), pn & 1, abort_flag, args.status);
+                ok = wait_warp(ptx::smem_u32(&cb->p_half[t]), pn & 1, abort_flag, args.status, args.wait_limit_ns);
                 if (!ok) break;
                 ptx::tc_fence_after();
                 issue_pv_h(v_ring + vs * C::v_slot_bytes, j == 0, 0);
               }
-              ok = wait_warp(ptx::smem_u32(&cb->p_full[t]), pn & 1, abort_flag, args.status);
+              ok = wait_warp(ptx::smem_u32(&cb->p_full[t]), pn & 1, abort_flag, args.status, args.wait_limit_ns);
               ++pn;
               if (!ok) break;
               ptx::tc_fence_after();
@@ -1036,7 +1093,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         // Drain: every MMA issued by either issuer completes before TMEM is
         // freed (the barrier expects one arrival from each issuer).
         ptx::mma_commit_elect(ptx::smem_u32(&cb->drain));
-        wait_warp(ptx::smem_u32(&cb->drain), 0, abort_flag, args.status);
+        wait_drain_warp(ptx::smem_u32(&cb->drain), 0, args.status);
       }
     }
   } else {
@@ -1096,7 +1153,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
       float m_used = neg_inf;  // running max, scaled log2 units
       float l = 0.f;
       for (int j = 0; j < w.n_kv; ++j) {
-        ok = wait_warp(ptx::smem_u32(&cb->s_full[t]), sn & 1, abort_flag, args.status);
+        ok = wait_warp(ptx::smem_u32(&cb->s_full[t]), sn & 1, abort_flag, args.status, args.wait_limit_ns);
         ++sn;
         if (!ok) break;
         ptx::tc_fence_after();
@@ -1206,7 +1263,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         // TMEM for the cluster combine, and (m, l) go into the row's first
         // two S/P columns, dead once the last P V (before o_full) is done.
         if (w.n_kv > 0) {
-          ok = wait_warp(ptx::smem_u32(&cb->o_full[t]), on & 1, abort_flag, args.status);
+          ok = wait_warp(ptx::smem_u32(&cb->o_full[t]), on & 1, abort_flag, args.status, args.wait_limit_ns);
           ++on;
           if (!ok) break;
           ptx::tc_fence_after();
@@ -1220,7 +1277,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
       // ---- epilogue: O / l -> bf16 rows, LSE
       uint32_t o[C::pv_n];
       if (w.n_kv > 0) {
-        ok = wait_warp(ptx::smem_u32(&cb->o_full[t]), on & 1, abort_flag, args.status);
+        ok = wait_warp(ptx::smem_u32(&cb->o_full[t]), on & 1, abort_flag, args.status, args.wait_limit_ns);
         ++on;
         if (!ok) break;
         ptx::tc_fence_after();
