@@ -17,7 +17,7 @@ from test_gpu_varlen import compare, make
 
 pytestmark = pytest.mark.gpu
 
-SHORT_NS = 2000  # a few pipeline hand-overs' worth
+SHORT_NS = 1000  # shorter than a load from HBM plus an MMA group
 
 
 def _varlen_case():

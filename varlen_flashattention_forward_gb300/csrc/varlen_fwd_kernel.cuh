@@ -370,8 +370,8 @@ static_assert(kMaxBatch < (1 << kUnitShift), "unit encoding");
 // microseconds; hitting the limit means the pipeline is broken.  The kernel
 // then records kStatusTimeout, raises the CTA abort flag and unwinds instead
 // of hanging.  Limits below kShortWaitNs (a test setting) poll with the
-// non-blocking probe and read the clock on every poll, so that a wait longer
-// than the limit always runs out.
+// non-blocking probe from the first attempt and read the clock on every
+// poll, so that a wait longer than the limit always runs out.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint64_t kShortWaitNs = 1000000ull;
 // Limit of the unwind's own waits (for the copies and MMAs a CTA started),
@@ -381,9 +381,8 @@ constexpr uint64_t kDrainLimitNs = 4000000000ull;
 __device__ __forceinline__ bool wait_single(uint32_t bar, uint32_t parity,
                                             volatile int* abort_flag, unsigned int* status,
                                             uint64_t limit_ns) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer_ns();
   if (limit_ns < kShortWaitNs) {
+    const uint64_t t0 = ptx::globaltimer_ns();
     for (;;) {
       if (ptx::mbar_test_wait(bar, parity)) return true;
       if (*abort_flag) return false;
@@ -394,6 +393,8 @@ __device__ __forceinline__ bool wait_single(uint32_t bar, uint32_t parity,
       }
     }
   }
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t spin = 1;; ++spin) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if ((spin & 255u) == 0) {
@@ -413,9 +414,9 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
                                           volatile int* abort_flag, unsigned int* status,
                                           uint64_t limit_ns) {
   const unsigned full = 0xffffffffu;
-  if (__all_sync(full, ptx::mbar_try_wait(bar, parity))) return true;
-  const uint64_t t0 = ptx::globaltimer_ns();
   const bool short_limit = limit_ns < kShortWaitNs;
+  if (!short_limit && __all_sync(full, ptx::mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t spin = 1;; ++spin) {
     const bool done = short_limit ? ptx::mbar_test_wait(bar, parity) : ptx::mbar_try_wait(bar, parity);
     if (__all_sync(full, done)) return true;
