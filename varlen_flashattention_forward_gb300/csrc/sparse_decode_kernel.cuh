@@ -332,6 +332,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const int ptid = tid - 128;
     const int u = ptid & 7;
     const uint64_t read_once = ptx::make_policy_evict_first();  // each row is read once
+    test_load_delay(a.wait_limit_ns);
     bool ok = true;
     for (int i = 0; i < n && ok; ++i) {
       const int st = i & 1;

@@ -369,9 +369,8 @@ static_assert(kMaxBatch < (1 << kUnitShift), "unit encoding");
 // kWaitLimitNs; fa_set_wait_limit_ns changes it).  Normal waits are
 // microseconds; hitting the limit means the pipeline is broken.  The kernel
 // then records kStatusTimeout, raises the CTA abort flag and unwinds instead
-// of hanging.  Limits below kShortWaitNs (a test setting) poll with the
-// non-blocking probe from the first attempt and read the clock on every
-// poll, so that a wait longer than the limit always runs out.
+// of hanging.  Waits read the clock every 256 probes, or on every probe
+// under limits below kShortWaitNs (a test setting, see test_load_delay).
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint64_t kShortWaitNs = 1000000ull;
 // Limit of the unwind's own waits (for the copies and MMAs a CTA started),
@@ -381,23 +380,11 @@ constexpr uint64_t kDrainLimitNs = 4000000000ull;
 __device__ __forceinline__ bool wait_single(uint32_t bar, uint32_t parity,
                                             volatile int* abort_flag, unsigned int* status,
                                             uint64_t limit_ns) {
-  if (limit_ns < kShortWaitNs) {
-    const uint64_t t0 = ptx::globaltimer_ns();
-    for (;;) {
-      if (ptx::mbar_test_wait(bar, parity)) return true;
-      if (*abort_flag) return false;
-      if (ptx::globaltimer_ns() - t0 > limit_ns) {
-        atomicOr(status, kStatusTimeout);
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t spin = 1;; ++spin) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((spin & 255u) == 0) {
+    if ((spin & 255u) == 0 || limit_ns < kShortWaitNs) {
       if (*abort_flag) return false;
       if (ptx::globaltimer_ns() - t0 > limit_ns) {
         atomicOr(status, kStatusTimeout);
@@ -414,13 +401,11 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
                                           volatile int* abort_flag, unsigned int* status,
                                           uint64_t limit_ns) {
   const unsigned full = 0xffffffffu;
-  const bool short_limit = limit_ns < kShortWaitNs;
-  if (!short_limit && __all_sync(full, ptx::mbar_try_wait(bar, parity))) return true;
+  if (__all_sync(full, ptx::mbar_try_wait(bar, parity))) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t spin = 1;; ++spin) {
-    const bool done = short_limit ? ptx::mbar_test_wait(bar, parity) : ptx::mbar_try_wait(bar, parity);
-    if (__all_sync(full, done)) return true;
-    if (short_limit || (spin & 255u) == 0) {
+    if (__all_sync(full, ptx::mbar_try_wait(bar, parity))) return true;
+    if ((spin & 255u) == 0 || limit_ns < kShortWaitNs) {
       int give_up = 0;
       if ((threadIdx.x & 31) == 0) {
         if (*abort_flag) {
@@ -434,6 +419,16 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
       if (__shfl_sync(full, give_up, 0)) return false;
     }
   }
+}
+
+// Under a test limit (below kShortWaitNs) the loaders pause this long before
+// their first copy, so that the first waits for their data outlast any
+// suspension inside try_wait and run out; bounded like every wait.
+constexpr uint64_t kTestLoadDelayNs = 50000000ull;
+__device__ __forceinline__ void test_load_delay(uint64_t limit_ns) {
+  if (limit_ns >= kShortWaitNs) return;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (ptx::globaltimer_ns() - t0 < kTestLoadDelayNs) __nanosleep(10000);
 }
 
 // The unwind's waits: for copies and MMAs this CTA started, which complete
@@ -842,6 +837,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     if (warp == kProducerWarp) {
       // ---------------------------------------------------------- producer
       if (lane == 0) {
+        test_load_delay(args.wait_limit_ns);
         // Per Q buffer b = 2 * pair + tile, bit b: parity of the q_free
         // phases consumed, of the Q loads issued, and whether any was issued.
         uint32_t qf_par = 0, qi_par = 0, qi_any = 0;
