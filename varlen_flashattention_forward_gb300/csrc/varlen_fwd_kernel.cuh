@@ -169,9 +169,6 @@ struct VarlenCfg {
   // P V -> S -> softmax by the half's tensor time).  Measured: ViT d80 +1 %;
   // d_v = 128 (ViT d128, MLA) -3 %, where the extra handover costs more.
   static constexpr bool split_pv = D_V <= 80;
-  // Part of the softmax exponentials on the FMA pipe (exp2_poly) for the
-  // head dims whose MMA group is short against the softmax.
-  static constexpr bool exp_poly = D_V <= 80;
   // TMEM columns of the S/P and O regions of query tile t.
   __host__ __device__ static constexpr uint32_t s_col(int t) { return 128u * (uint32_t)t; }
   __host__ __device__ static constexpr uint32_t o_col(int t) { return 256u + 128u * (uint32_t)t; }
@@ -236,40 +233,6 @@ __device__ __forceinline__ uint32_t ring_slot(uint32_t n) {
   uint32_t s = n % (uint32_t)Size;
   if (Size == 1) asm volatile("" : "+r"(s));
   return s;
-}
-
-// ------------------------------------------------------------ exp2 on the FMA pipe
-// 2^x for an element pair without the MUFU unit: x = n + f with n the
-// nearest integer (adding and subtracting 1.5 * 2^23 rounds in fp32), f in
-// [-1/2, 1/2]; 2^f by a degree-3 minimax polynomial (relative error 7.5e-5,
-// fitted by the Remez exchange algorithm in exp2_poly.py beside this
-// package); 2^n added to the exponent field.  x is clamped at -125 so that
-// the exponent stays normal (2^-125 is far below what a bf16 P or the row
-// sum resolve); only tiles with no masked key use it, so x is never -inf.
-constexpr int kPolyEvery = 4;  // one element pair in four
-constexpr float kExp2C0 = 9.999280572e-01f;  // kExp2Cn multiplies f^n
-constexpr float kExp2C1 = 6.932609677e-01f;
-constexpr float kExp2C2 = 2.426111251e-01f;
-constexpr float kExp2C3 = 5.517166853e-02f;
-__device__ __forceinline__ uint64_t exp2_poly(uint64_t x2) {
-  float x0, x1;
-  ptx::f2_unpack(x2, x0, x1);
-  const uint64_t xc = ptx::f2_pack(fmaxf(x0, -125.f), fmaxf(x1, -125.f));
-  const float kMagic = 12582912.0f;  // 1.5 * 2^23
-  const uint64_t t = ptx::add2(xc, ptx::f2_pack(kMagic, kMagic));
-  const uint64_t n = ptx::add2(t, ptx::f2_pack(-kMagic, -kMagic));
-  const uint64_t f = ptx::fma2(n, ptx::f2_pack(-1.f, -1.f), xc);
-  uint64_t p = ptx::fma2(ptx::f2_pack(kExp2C3, kExp2C3), f, ptx::f2_pack(kExp2C2, kExp2C2));
-  p = ptx::fma2(p, f, ptx::f2_pack(kExp2C1, kExp2C1));
-  p = ptx::fma2(p, f, ptx::f2_pack(kExp2C0, kExp2C0));
-  float p0, p1, t0, t1;
-  ptx::f2_unpack(p, p0, p1);
-  ptx::f2_unpack(t, t0, t1);
-  // The low bits of t hold n (two's complement): n << 23 lands on the
-  // exponent field, the bits of 1.5 * 2^23 shift out.
-  p0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
-  p1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
-  return ptx::f2_pack(p0, p1);
 }
 
 // ------------------------------------------------------------ MMA groups
@@ -1204,8 +1167,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
 
         const int k0 = (w.tile_lo + j) * kBN;
         float row_max;
-        const bool whole_tile = k0 >= lo_i && k0 + kBN <= hi_i;
-        if (whole_tile) {
+        if (k0 >= lo_i && k0 + kBN <= hi_i) {
           // Every key of the tile is visible to this row: the hardware max.
           row_max = ptx::max3(qmax[0], qmax[1], fmaxf(qmax[2], qmax[3]));
         } else {
@@ -1258,46 +1220,28 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         uint32_t pr[kBN / 2];
         {
           uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
-          // Keys [c0, c0 + 64): exp2, row sum, P as bf16 pairs.  With POLY,
-          // one element pair in kPolyEvery goes through exp2_poly on the
-          // FMA pipe instead of the MUFU unit.
-          auto exp_half = [&](auto half, auto poly) {
+          // Keys [c0, c0 + 64): exp2, row sum, P as bf16 pairs.
+          auto exp_half = [&](auto half) {
             constexpr int c0 = decltype(half)::value * (kBN / 2);
-            constexpr bool POLY = decltype(poly)::value != 0;
 #pragma unroll
             for (int c = c0; c < c0 + kBN / 2; c += 2) {
-              const uint64_t x2 = ptx::fma2(ptx::f2_pack(s[c], s[c + 1]), sl2x2, nbx2);
-              float p0, p1;
-              if (POLY && ((c >> 1) % kPolyEvery) == kPolyEvery - 1) {
-                ptx::f2_unpack(exp2_poly(x2), p0, p1);
-              } else {
-                float x0, x1;
-                ptx::f2_unpack(x2, x0, x1);
-                p0 = ptx::ex2(x0);
-                p1 = ptx::ex2(x1);
-              }
+              float x0, x1;
+              ptx::f2_unpack(ptx::fma2(ptx::f2_pack(s[c], s[c + 1]), sl2x2, nbx2), x0, x1);
+              const float p0 = ptx::ex2(x0);
+              const float p1 = ptx::ex2(x1);
               ls2[(c >> 1) & 3] = ptx::add2(ls2[(c >> 1) & 3], ptx::f2_pack(p0, p1));
               pr[c >> 1] = ptx::pack_bf16x2(p0, p1);
             }
           };
-          // The polynomial only where every row of the warp sees the whole
-          // tile (no -inf), and for head dims whose softmax limits the
-          // kernel (C::exp_poly).
-          auto exp_tile = [&](auto poly) {
-            exp_half(IntTag<0>{}, poly);
-            if (C::split_pv) {
-              // The first 64 keys' P goes out before the rest is computed.
-              ptx::tmem_st32(s_addr, pr);
-              ptx::tmem_wait_st();
-              ptx::tc_fence_before();
-              ptx::mbar_arrive(ptx::smem_u32(&cb->p_half[t]));
-            }
-            exp_half(IntTag<1>{}, poly);
-          };
-          if (C::exp_poly && __all_sync(0xffffffffu, whole_tile))
-            exp_tile(IntTag<1>{});
-          else
-            exp_tile(IntTag<0>{});
+          exp_half(IntTag<0>{});
+          if (C::split_pv) {
+            // The first 64 keys' P goes out before the rest is computed.
+            ptx::tmem_st32(s_addr, pr);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(ptx::smem_u32(&cb->p_half[t]));
+          }
+          exp_half(IntTag<1>{});
           float a0, a1, b0, b1;
           ptx::f2_unpack(ptx::add2(ls2[0], ls2[1]), a0, a1);
           ptx::f2_unpack(ptx::add2(ls2[2], ls2[3]), b0, b1);
