@@ -155,13 +155,6 @@ struct VarlenCfg {
   static constexpr int nv = min_(8, nk + ((ring_bytes(q_pairs) - nk * (k_slot_bytes + v_slot_bytes)) /
                                           v_slot_bytes > 0 ? 1 : 0));
   static_assert(nk >= 1 && nv >= 2, "shared memory too small for the K and V rings");
-  // A one-slot K ring (d_qk = 192) is filled and released per 64-wide
-  // column chunk, each with its own barrier pair: both issuers release a
-  // chunk as soon as their MMAs on it are done, so the next K tile's first
-  // chunks load while the last chunks of the current one are still read.
-  static constexpr bool chunk_k = nk == 1;
-  static constexpr int k_bars = chunk_k ? QK::chunks : nk;
-  static_assert(k_bars <= 8, "K ring barriers");
   static_assert(pv_n <= 128, "O accumulator wider than its TMEM region");
   // Issue order between the two query tiles' MMA groups.  Strict turns
   // (ping-pong) for d_qk == d_v, where a group is short and free-running
@@ -293,27 +286,6 @@ __device__ __forceinline__ void issue_s_group(uint32_t d, uint64_t qd, uint64_t 
                  "}\n" FA_S_OPERANDS);
   } else {
     static_assert(FULL < 0, "head dimension without an S issue group");
-  }
-#undef FA_S_OPERANDS
-}
-
-// One 64-wide chunk C of S_t = Q_t K_j^T (four K=16 steps), for the chunked
-// K ring: chunk 0 overwrites S, the others accumulate.
-template <int C>
-__device__ __forceinline__ void issue_s_chunk(uint32_t d, uint64_t qd, uint64_t kd,
-                                              uint32_t idesc) {
-  constexpr uint32_t kChunk = (uint32_t)(kBN * 128) >> 4;  // chunk distance, 16-byte units
-#define FA_S_OPERANDS                                                                   \
-  ::"r"(d), "l"(qd), "l"(kd), "l"(qd), "l"(kd), "r"(idesc), "n"(kChunk), "r"(1u) \
-      : "memory"
-  if constexpr (C == 0) {
-    asm volatile(FA_GROUP_BEGIN FA_SS_CHUNK(0, "pz") "}\n" FA_S_OPERANDS);
-  } else if constexpr (C == 1) {
-    asm volatile(FA_GROUP_BEGIN FA_SS_CHUNK(1, "pa") "}\n" FA_S_OPERANDS);
-  } else if constexpr (C == 2) {
-    asm volatile(FA_GROUP_BEGIN FA_SS_CHUNK(2, "pa") "}\n" FA_S_OPERANDS);
-  } else {
-    static_assert(C < 0, "chunk without an S issue group");
   }
 #undef FA_S_OPERANDS
 }
@@ -822,7 +794,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     ptx::mbar_init(ptx::smem_u32(&cb->drain), 2);
     ptx::mbar_init(ptx::smem_u32(&cb->turn[0]), 1);
     ptx::mbar_init(ptx::smem_u32(&cb->turn[1]), 1);
-    for (int s = 0; s < C::k_bars; ++s) {
+    for (int s = 0; s < NK; ++s) {
       ptx::mbar_init(ptx::smem_u32(&cb->k_full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&cb->k_free[s]), 2);  // one release per issuer
     }
@@ -873,7 +845,6 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         // Tiles loaded into each ring so far: tile n goes to slot n % size,
         // fill parity (n / size) & 1.
         uint32_t kn = 0, vn = 0;
-        int kc_issued = 0;  // chunks of K tile kn already issued (chunked K ring)
         bool ok = true;
         for (int r = 0; r * (int)gridDim.x < total_items && ok; ++r) {
           const int it = snake_item(r, split);
@@ -903,30 +874,11 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           for (int j = 0; j < w.n_kv && ok; ++j) {
             const int krow = w.k_start + (w.tile_lo + j) * kBN;
             // K_j into the K ring.
-            if constexpr (C::chunk_k) {
-              // Chunk by chunk into the single slot, each on its own barrier.
-              for (int c = 0; c < QK::chunks && ok; ++c) {
-                ok = wait_single(ptx::smem_u32(&cb->k_free[c]), (kn & 1) ^ 1, abort_flag,
-                                 args.status, args.wait_limit_ns);
-                if (!ok) break;
-                const uint32_t bar = ptx::smem_u32(&cb->k_full[c]);
-                ptx::mbar_arrive_expect_tx(bar, kBN * QK::chunk_width(c) * 2);
-                ptx::tma_load_3d(ptx::smem_u32(k_ring + QK::chunk_off(c, kBN)),
-                                 c < QK::full ? &maps.k_full : &maps.k_tail, bar, c * 64,
-                                 w.kv_head, krow);
-                kc_issued = c + 1;
-              }
-              if (!ok) break;
-              ++kn;
-              kc_issued = 0;
-            }
             const uint32_t ks = ring_slot<NK>(kn);
-            if (!C::chunk_k) {
-              ok = wait_single(ptx::smem_u32(&cb->k_free[ks]), ((kn / NK) & 1) ^ 1, abort_flag,
-                               args.status, args.wait_limit_ns);
-            }
+            ok = wait_single(ptx::smem_u32(&cb->k_free[ks]), ((kn / NK) & 1) ^ 1, abort_flag,
+                             args.status, args.wait_limit_ns);
             if (!ok) break;
-            if (!C::chunk_k) {
+            {
               const uint32_t bar = ptx::smem_u32(&cb->k_full[ks]);
               uint8_t* dst = k_ring + ks * C::k_slot_bytes;
               ptx::mbar_arrive_expect_tx(bar, C::k_tile_bytes);
@@ -961,19 +913,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
               wait_drain_single(ptx::smem_u32(&cb->q_full[b]), ((qi_par >> b) & 1) ^ 1,
                                 args.status);
           // Slot s was last filled by tile s + size * ((n - 1 - s) / size).
-          if constexpr (C::chunk_k) {
-            // Chunk c was last filled for tile kn if it was issued before the
-            // abort, else for tile kn - 1.
-            for (int c = 0; c < QK::chunks; ++c) {
-              const int last = c < kc_issued ? (int)kn : (int)kn - 1;
-              if (last >= 0)
-                wait_drain_single(ptx::smem_u32(&cb->k_full[c]), (uint32_t)last & 1, args.status);
-            }
-          } else {
-            for (uint32_t s = 0; s < (uint32_t)NK && s < kn; ++s)
-              wait_drain_single(ptx::smem_u32(&cb->k_full[s]), ((kn - 1 - s) / NK) & 1,
-                                args.status);
-          }
+          for (uint32_t s = 0; s < (uint32_t)NK && s < kn; ++s)
+            wait_drain_single(ptx::smem_u32(&cb->k_full[s]), ((kn - 1 - s) / NK) & 1,
+                              args.status);
           for (uint32_t s = 0; s < (uint32_t)NV && s < vn; ++s)
             wait_drain_single(ptx::smem_u32(&cb->v_full[s]), ((vn - 1 - s) / NV) & 1,
                               args.status);
@@ -1024,31 +966,6 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           issue_s_group<QK::full, QK::tail>(tmem + C::s_col(t), q_desc, kd, q_desc_tail, kd_tail,
                                             idesc_s);
         };
-        // Chunked K ring: S_t(j) chunk by chunk as each lands, each chunk
-        // released (commit) right after its MMAs; both issuers release every
-        // chunk (an issuer without a tile in the item only waits).
-        auto s_chunked = [&](bool issue) -> bool {
-          bool good = true;
-          auto chunk = [&](auto cc) {
-            constexpr int c = decltype(cc)::value;
-            if (!good) return;
-            good = wait_warp(ptx::smem_u32(&cb->k_full[c]), kn & 1, abort_flag, args.status,
-                             args.wait_limit_ns);
-            if (!good) return;
-            ptx::tc_fence_after();
-            if (issue) {
-              const uint32_t ka = ptx::smem_u32(k_ring);
-              issue_s_chunk<c>(tmem + C::s_col(t), q_desc,
-                               ptx::smem_desc(ka, 16, 1024, ptx::kLayoutSw128), idesc_s);
-            }
-            ptx::mma_commit_elect(ptx::smem_u32(&cb->k_free[c]));
-          };
-          chunk(IntTag<0>{});
-          if constexpr (QK::chunks > 1) chunk(IntTag<1>{});
-          if constexpr (QK::chunks > 2) chunk(IntTag<2>{});
-          ++kn;
-          return good;
-        };
         auto issue_pv = [&](const uint8_t* vbuf, bool first) {
           // One MMA per 16 keys over all of d_v: MN-major B spanning
           // C::v_atoms atoms (LBO = atom stride), 8-key groups SBO apart.
@@ -1087,16 +1004,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             set_q(qb);
           }
           // Prologue: S_t(0).
-          if constexpr (C::chunk_k) {
-            ok = take_turn() && s_chunked(mine);
-            if (!ok) break;
-            pass_turn();
-            if (mine) {
-              ptx::mma_commit_elect(ptx::smem_u32(&cb->s_full[t]));
-              if (!C::stage_o && w.n_kv == 1)
-                ptx::mma_commit_elect(ptx::smem_u32(&cb->q_free[qb]));
-            }
-          } else {
+          {
             const uint32_t ks = ring_slot<NK>(kn);
             ok = wait_warp(ptx::smem_u32(&cb->k_full[ks]), (kn / NK) & 1, abort_flag,
                            args.status, args.wait_limit_ns);
@@ -1160,19 +1068,12 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
               else
                 issue_pv(v_ring + vs * C::v_slot_bytes, j == 0);
             }
-            if constexpr (C::chunk_k) {
-              if (has_next) {
-                ok = s_chunked(mine);
-                if (!ok) break;
-              }
-            } else {
-              if (!kEarlyK && has_next) {
-                ok = wait_k();
-                if (!ok) break;
-                ptx::tc_fence_after();
-              }
-              if (mine && has_next) issue_s(k_ring + ks * C::k_slot_bytes);
+            if (!kEarlyK && has_next) {
+              ok = wait_k();
+              if (!ok) break;
+              ptx::tc_fence_after();
             }
+            if (mine && has_next) issue_s(k_ring + ks * C::k_slot_bytes);
             // The other issuer goes next, then the commits (a commit tracks
             // this thread's MMAs alone; issuing one costs the warp time that
             // would otherwise delay the other query tile's MMAs).
@@ -1182,7 +1083,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
               if (!C::stage_o && j + 2 == w.n_kv)
                 ptx::mma_commit_elect(ptx::smem_u32(&cb->q_free[qb]));
             }
-            if (!C::chunk_k && has_next) ptx::mma_commit_elect(ptx::smem_u32(&cb->k_free[ks]));
+            if (has_next) ptx::mma_commit_elect(ptx::smem_u32(&cb->k_free[ks]));
             ptx::mma_commit_elect(ptx::smem_u32(&cb->v_free[vs]));
           }
         }
