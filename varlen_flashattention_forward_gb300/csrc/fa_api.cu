@@ -319,6 +319,18 @@ extern "C" fa_status fa_varlen_fwd_strided(
     ok = encode_rows(&maps.q_tail, q, d_qk, num_heads, total_q, qt, fa::kBM / qh, q_head_stride,
                      q_row_stride, qh) &&
          encode_rows(&maps.k_tail, kb, d_qk, kh, tk, qt, fa::kBN, khs, krs);
+  if (ok) {
+    // O as [total_q, H, d_v] through boxes of {d_v, 1, 128}, no swizzle.
+    EncodeTiledFn fn = encode_fn();
+    cuuint64_t dims[3] = {(cuuint64_t)d_v, (cuuint64_t)num_heads, (cuuint64_t)total_q};
+    cuuint64_t strides[2] = {(cuuint64_t)d_v * 2, (cuuint64_t)num_heads * d_v * 2};
+    cuuint32_t box[3] = {(cuuint32_t)d_v, 1u, (cuuint32_t)fa::kBM};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    ok = fn && fn(&maps.o_rows, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+                     CUDA_SUCCESS;
+  }
   if (!ok) return FA_ERR_LAUNCH;
 
   fa::VarlenArgs args;

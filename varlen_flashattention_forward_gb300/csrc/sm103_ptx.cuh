@@ -119,6 +119,17 @@ __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t byt
                "r"(src), "r"(bytes)
                : "memory");
 }
+// 3-D tiled bulk tensor store shared -> global of one box of the tensor
+// map at the given element coordinates (innermost first), tracked in this
+// thread's bulk async-group.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int32_t c0,
+                                             int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(src)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
