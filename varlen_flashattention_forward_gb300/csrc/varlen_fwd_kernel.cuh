@@ -351,6 +351,22 @@ struct WorkItem {
 };
 // Row r of a work item (0 .. 255) is token row0 + (r >> pack_shift) of the
 // sequence and query head head + r % P.
+static_assert(sizeof(WorkItem) == 48, "work item slot size");
+
+// Decoded work items, published by the producer (which runs ahead of the
+// other roles) into a ring in shared memory: decoding an item (a search of
+// the work list, reads of cu_seqlens, integer divisions) costs about 1000
+// cycles, which the MMA issuers and softmax warps would otherwise spend at
+// every item boundary.  Lives in the work-list scan's scratch (s_part), dead
+// once the list is built.
+constexpr int kItemSlots = 4;
+constexpr int kItemReaders = 2 + 8;  // the issuer warps and the softmax warps
+struct ItemRing {
+  WorkItem slot[kItemSlots];
+  uint64_t full[kItemSlots];
+  uint64_t free_[kItemSlots];
+};
+static_assert(sizeof(ItemRing) <= 4 * kVarlenThreads, "item ring fits the scan scratch");
 
 // Short segments: consecutive sequences of 1..kPackMaxLen query rows with as
 // many keys and the same token offsets in Q and K (self-attention over one
@@ -775,9 +791,11 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
   uint8_t* k_ring = smem + 2 * C::q_pairs * C::q_tile_bytes;
   uint8_t* v_ring = k_ring + NK * C::k_slot_bytes;
   VarlenBarriers* cb = reinterpret_cast<VarlenBarriers*>(v_ring + NV * C::v_slot_bytes);
-  int* s_prefix = reinterpret_cast<int*>(cb + 1);
+  // The scan scratch first (a fixed offset from the shared-memory base: the
+  // decoded-item ring lives there once the list is built), then the list.
+  int* s_part = reinterpret_cast<int*>(cb + 1);
+  int* s_prefix = s_part + kVarlenThreads;
   int* s_sorted = s_prefix + (args.batch + 1);
-  int* s_part = s_sorted + args.batch;
   volatile int* abort_flag = &cb->abort_flag;
 
   const int tid = threadIdx.x;
@@ -831,11 +849,21 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
   build_work_list(args.cu_q, args.cu_k, args.batch, args.num_heads, pshift, s_prefix,
                   s_sorted, s_part,
                   reinterpret_cast<int*>(k_ring));  // ends with __syncthreads
+  if (tid == 0) {
+    // The decoded-item ring, in the scan scratch the list builder is done with.
+    ItemRing* rg = reinterpret_cast<ItemRing*>(s_part);
+    for (int sl = 0; sl < kItemSlots; ++sl) {
+      ptx::mbar_init(ptx::smem_u32(&rg->full[sl]), 1);
+      ptx::mbar_init(ptx::smem_u32(&rg->free_[sl]), kItemReaders);
+    }
+    ptx::fence_mbar_init();
+  }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = cb->tmem_base;
   const int total_items = s_prefix[args.batch];
+  ItemRing* const ring = reinterpret_cast<ItemRing*>(s_part);
 
   if (warp >= 8) {
     ptx::regs_dec<kControlRegs>();
@@ -855,6 +883,18 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           const int it = snake_item(r, split);
           if (it >= total_items) continue;
           const WorkItem w = decode_item(it, args, s_prefix, s_sorted, split, pshift);
+          {
+            // Publish the item (every one, empty or not: all roles walk the
+            // same sequence).
+            // Item of round r (only the last round can be without one, so r
+            // counts the items of every role).
+            const uint32_t sl = (uint32_t)r % kItemSlots;
+            ok = wait_single(ptx::smem_u32(&ring->free_[sl]), (((uint32_t)r / kItemSlots) & 1) ^ 1,
+                             abort_flag, args.status, args.wait_limit_ns);
+            if (!ok) break;
+            ring->slot[sl] = w;
+            ptx::mbar_arrive(ptx::smem_u32(&ring->full[sl]));
+          }
           if (w.n_kv == 0) continue;
           const int pair = C::q_pairs == 2 ? (int)(item_n & 1) : 0;
           ++item_n;
@@ -996,7 +1036,15 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         for (int r = 0; r * (int)gridDim.x < total_items && ok; ++r) {
           const int it = snake_item(r, split);
           if (it >= total_items) continue;
-          const WorkItem w = decode_item(it, args, s_prefix, s_sorted, split, pshift);
+          WorkItem w;
+          {
+            const uint32_t sl = (uint32_t)r % kItemSlots;
+            ok = wait_warp(ptx::smem_u32(&ring->full[sl]), ((uint32_t)r / kItemSlots) & 1,
+                           abort_flag, args.status, args.wait_limit_ns);
+            if (!ok) break;
+            w = ring->slot[sl];
+            ptx::mbar_arrive_elect(ptx::smem_u32(&ring->free_[sl]));
+          }
           if (w.n_kv == 0) continue;
           const bool mine = t < w.n_qt;
           const int qb = 2 * (C::q_pairs == 2 ? (int)(item_n & 1) : 0) + t;  // Q buffer
@@ -1124,7 +1172,16 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     for (int r = 0; r * (int)gridDim.x < total_items && ok; ++r) {
       const int it = snake_item(r, split);
       if (it >= total_items) continue;
-      const WorkItem w = decode_item(it, args, s_prefix, s_sorted, split, pshift);
+      WorkItem w;
+      {
+        const uint32_t sl = (uint32_t)r % kItemSlots;
+        ok = wait_warp(ptx::smem_u32(&ring->full[sl]), ((uint32_t)r / kItemSlots) & 1, abort_flag,
+                       args.status, args.wait_limit_ns);
+        if (!ok) break;
+        w = ring->slot[sl];
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ring->free_[sl]));
+      }
       const int qb = 2 * (C::q_pairs == 2 ? (int)(item_n & 1) : 0) + t;  // this item's Q buffer
       if (w.n_kv > 0) ++item_n;
       if (t >= w.n_qt) continue;
