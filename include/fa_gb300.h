@@ -200,8 +200,10 @@ fa_status fa_varlen_fwd_strided(const void* q, long long q_row_stride, long long
  *                 A slot with p < 0, p >= 64*max_pages_per_tok or a page id
  *                 outside [0, num_pages) is skipped (contributes nothing).
  *   num_heads     one of 8, 16, 32, 64, 128
- *   topk          multiple of 128, 128 .. min(2048, 64*max_pages_per_tok)
- *                 (the per-token row table is held in shared memory)
+ *   topk          multiple of 128, 128 .. 64*max_pages_per_tok.  A CTA
+ *                 takes at most 2048 key slots (its row table is held in
+ *                 shared memory), so a token with a larger top-k is always
+ *                 cut between CTAs and merged.
  *   softmax_scale scale of the 576-wide dot product (> 0)
  *   out           bf16 [num_tokens, num_heads, 512]: sum_j p_j * row_j[0:512]
  *   lse           fp32 [num_heads, num_tokens] or NULL
@@ -221,7 +223,9 @@ fa_status fa_varlen_fwd_strided(const void* q, long long q_row_stride, long long
  * that is to contain a call.  Calls on one stream share its workspace in
  * stream order.  Per-thread default streams of different host threads share
  * one workspace per device, so they must not run decode calls at the same
- * time.  At most two waves of CTAs split (about 80 MB on 152 SMs).
+ * time.  Up to top-k 2048 the split is used for at most two waves of CTAs
+ * (a workspace of about 80 MB on 152 SMs); a larger top-k always splits,
+ * and its workspace is 2 x CTAs x 131 KB (fa_sparse_mla_decode_plan).
  *
  * Host errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (heads, topk),
  * FA_ERR_ARCH, FA_ERR_LAUNCH (launch or workspace allocation failed).

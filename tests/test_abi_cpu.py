@@ -137,7 +137,8 @@ def decode(lib, **kw):
     (dict(c=P(0x2004)), fa.FA_ERR_INVALID_ARG),
     (dict(H=48), fa.FA_ERR_UNSUPPORTED),
     (dict(topk=200), fa.FA_ERR_UNSUPPORTED),
-    (dict(topk=2048, maxp=16), fa.FA_ERR_UNSUPPORTED),
+    (dict(topk=2048, maxp=16), fa.FA_ERR_UNSUPPORTED),   # more slots than the context
+    (dict(topk=1100, maxp=64), fa.FA_ERR_UNSUPPORTED),   # not a multiple of 128
 ])
 def test_decode_host_validation(lib, kw, expect):
     assert decode(lib, **kw) == expect
@@ -158,7 +159,8 @@ def test_valid_arguments_without_gpu_fail_cleanly(lib):
     ((-1, 64, 256, True, True), fa.FA_ERR_INVALID_ARG),
     ((4, 48, 256, True, True), fa.FA_ERR_UNSUPPORTED),
     ((4, 64, 200, True, True), fa.FA_ERR_UNSUPPORTED),
-    ((4, 64, 4096, True, True), fa.FA_ERR_UNSUPPORTED),
+    ((4, 64, 4100, True, True), fa.FA_ERR_UNSUPPORTED),
+    ((4, 64, 8192, True, True), None),             # above 2048: always split
 ])
 def test_decode_plan_host_validation(lib, args, expect):
     import torch

@@ -127,3 +127,17 @@ def test_split_with_invalid_part(cuda_device):
     ti = ti.clone()
     ti[0, 128:256] = -1   # tiles 2-3 (one CTA's whole range) invalid
     compare(q, cache, pt, ti, scale)
+
+
+@pytest.mark.parametrize("T,H,topk,context", [(2, 64, 4096, 8192), (3, 128, 8192, 16384),
+                                              (1, 16, 2176, 4096)])
+def test_topk_above_one_cta_range(cuda_device, T, H, topk, context):
+    # A CTA holds at most 2048 key slots: a larger top-k is always cut
+    # between CTAs and merged (many parts per token).
+    launches, ws = fa.fa_sparse_mla_decode_plan(T, H, topk)
+    assert launches == 2 and ws > 0
+    q, cache, pt, ti, scale = small_inputs(T, H, topk, context, seed=topk + T)
+    compare(q, cache, pt, ti, scale)
+    a = run_gpu(q, cache, pt, ti, scale)
+    b = run_gpu(q, cache, pt, ti, scale)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])

@@ -417,6 +417,15 @@ struct DecodeSplit {
 DecodeSplit decode_split(long long units, int n_tiles, long long sms) {
   auto ceil_div = [](long long x, long long y) { return (x + y - 1) / y; };
   const long long total = units * n_tiles;
+  if (n_tiles > fa::kDecodeMaxTilesPerCta) {
+    // A unit longer than one CTA's range (top-k above 2048): always the
+    // equal-tile cut, over as many waves as it takes.
+    DecodeSplit d;
+    d.grid = std::min(ceil_div(total, fa::kDecodeMaxTilesPerCta * sms) * sms, total / 2);
+    d.gran = 1;
+    d.split = true;
+    return d;
+  }
   // Whole units per CTA.
   const long long upc = fa::kDecodeMaxTilesPerCta / n_tiles;
   const long long grid_u = std::max(ceil_div(units, upc), std::min(units, sms));
@@ -466,8 +475,7 @@ fa_status plan_decode(const void* q, const void* kv_cache, const int* page_table
   if (num_heads != 8 && num_heads != 16 && num_heads != 32 && num_heads != 64 &&
       num_heads != 128)
     return FA_ERR_UNSUPPORTED;
-  if (topk % 128 != 0 || topk > fa::kDecodeMaxTopk ||
-      (int64_t)topk > (int64_t)max_pages_per_tok * fa::kDecodePage)
+  if (topk % 128 != 0 || (int64_t)topk > (int64_t)max_pages_per_tok * fa::kDecodePage)
     return FA_ERR_UNSUPPORTED;
   if ((int64_t)num_pages * fa::kDecodePage > INT32_MAX) return FA_ERR_UNSUPPORTED;
   const int groups = (num_heads + 63) / 64;
@@ -593,7 +601,7 @@ extern "C" fa_status fa_sparse_mla_decode_plan(int num_tokens, int num_heads, in
   if (num_heads != 8 && num_heads != 16 && num_heads != 32 && num_heads != 64 &&
       num_heads != 128)
     return FA_ERR_UNSUPPORTED;
-  if (topk % 128 != 0 || topk > fa::kDecodeMaxTopk) return FA_ERR_UNSUPPORTED;
+  if (topk % 128 != 0) return FA_ERR_UNSUPPORTED;
   const int groups = (num_heads + 63) / 64;
   const int n_tiles = topk / fa::kDecodeKeys;
   const long long units = (long long)num_tokens * groups;

@@ -67,7 +67,7 @@ constexpr uint32_t kDecodeSoftmaxRegs = 232;
 constexpr uint32_t kDecodeGatherRegs = 88;
 constexpr uint32_t kDecodeControlRegs = 96;
 constexpr int kDecodeKeys = 64;       // keys per tile
-constexpr int kDecodeMaxTopk = 2048;  // row table held in shared memory
+constexpr int kDecodeMaxTopk = 2048;  // key slots of one CTA's range (row table in shared memory)
 constexpr int kDecodeMaxTilesPerCta = kDecodeMaxTopk / 64;
 // Measured cost of a split schedule's partial writes, segment switches and
 // merge kernel, in tile times (one tile: ~2.7 us on one SM).
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const int lo = decode_cta_lo(a, blockIdx.x);
   const int n = decode_cta_lo(a, blockIdx.x + 1) - lo;
   // Tile i of the range is tile (pos0 + i) % n_tiles of unit
-  // unit0 + (pos0 + i) / n_tiles (32-bit: pos0 + i < 2 * kDecodeMaxTilesPerCta).
+  // unit0 + (pos0 + i) / n_tiles (32-bit: pos0 < n_tiles, i < kDecodeMaxTilesPerCta).
   const int pos0 = lo % n_tiles;
   const int unit0 = lo / n_tiles;
   auto seg_first = [&](int i) { return i == 0 || (pos0 + i) % n_tiles == 0; };
