@@ -169,6 +169,12 @@ struct VarlenCfg {
   // P V -> S -> softmax by the half's tensor time).  Measured: ViT d80 +1 %;
   // d_v = 128 (ViT d128, MLA) -3 %, where the extra handover costs more.
   static constexpr bool split_pv = D_V <= 80;
+  // Per-query-tile key ranges inside a work item (tile_kv_range) for the
+  // MLA shapes, whose prefill is causal or windowed: sliding window (1024,
+  // 0) 1287 -> 1214 us, causal 4 x 4096 2028 -> 1993 us.  The other head
+  // dims run the item's whole range for both tiles: their state cost the
+  // non-causal ViT and long-sequence loops 1-4 %.
+  static constexpr bool tile_ranges = D_QK != D_V;
   // TMEM columns of the S/P and O regions of query tile t.
   __host__ __device__ static constexpr uint32_t s_col(int t) { return 128u * (uint32_t)t; }
   __host__ __device__ static constexpr uint32_t o_col(int t) { return 256u + 128u * (uint32_t)t; }
@@ -667,6 +673,29 @@ __device__ __forceinline__ WorkItem decode_item(int it, const VarlenArgs& a,
   return w;
 }
 
+// Key tiles [jlo, jhi) of a work item (relative to its tile_lo) that query
+// tile t of the item can see: the causal and window bounds of the tile's
+// first and last rows.  The two query tiles of an item share its KV tiles
+// but not all of them (a causal tile 0 cannot see the diagonal tile of
+// tile 1; under a sliding window tile 1 cannot see the first tile of tile
+// 0); the issuer of tile t and its softmax warpgroup both walk exactly these
+// tiles.  Packs of short segments keep the item's whole range.
+__device__ __forceinline__ void tile_kv_range(const WorkItem& w, int t, int wl, int wr,
+                                              int pack_shift, int& jlo, int& jhi) {
+  jlo = 0;
+  jhi = w.n_kv;
+  if (w.nb > 1 || w.n_kv == 0) return;
+  const int off = w.lk - w.lq;
+  const int r0 = w.row0 + ((t * kBM) >> pack_shift);                        // first token
+  const int r1 = min(w.lq, w.row0 + (((t + 1) * kBM) >> pack_shift)) - 1;   // last token
+  if (wl >= 0) jlo = max(0, max(0, r0 + off - wl) / kBN - w.tile_lo);
+  if (wr >= 0) {
+    const int khi = min(w.lk, r1 + off + wr + 1);  // keys < khi
+    jhi = khi <= 0 ? 0 : min(w.n_kv, (khi + kBN - 1) / kBN - w.tile_lo);
+  }
+  if (jhi < jlo) jhi = jlo;
+}
+
 // ------------------------------------------------------------ split-KV combine
 // Split-KV partials in shared memory, in the Q tiles and K/V rings of the
 // item's CTAs (dead once the item's last MMA is done): row r of the item's
@@ -1047,6 +1076,15 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           }
           if (w.n_kv == 0) continue;
           const bool mine = t < w.n_qt;
+          // This tile's key tiles: S_t(j) for j in [jlo, jhi), issued at the
+          // step before (or in the prologue), P V_t(j) at step j.
+          int jlo = 0, jhi = 0;
+          if (mine) {
+            if (C::tile_ranges)
+              tile_kv_range(w, t, args.wl, args.wr, pshift, jlo, jhi);
+            else
+              jhi = w.n_kv;
+          }
           const int qb = 2 * (C::q_pairs == 2 ? (int)(item_n & 1) : 0) + t;  // Q buffer
           ++item_n;
           if (mine) {
@@ -1064,18 +1102,20 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             if (ok) ok = take_turn();
             if (!ok) break;
             ptx::tc_fence_after();
-            if (mine) issue_s(k_ring + ks * C::k_slot_bytes);
+            const bool s0 = jlo == 0 && jhi > 0;  // (jhi > jlo only for an owned tile)
+            if (s0) issue_s(k_ring + ks * C::k_slot_bytes);
             pass_turn();
-            if (mine) {
-              ptx::mma_commit_elect(ptx::smem_u32(&cb->s_full[t]));
-              if (!C::stage_o && w.n_kv == 1)
-                ptx::mma_commit_elect(ptx::smem_u32(&cb->q_free[qb]));
-            }
+            if (s0) ptx::mma_commit_elect(ptx::smem_u32(&cb->s_full[t]));
+            // Q is free once the tile's last S is done (or it has none).
+            if (!C::stage_o && mine && (jhi <= jlo || (s0 && jhi == 1)))
+              ptx::mma_commit_elect(ptx::smem_u32(&cb->q_free[qb]));
             ptx::mma_commit_elect(ptx::smem_u32(&cb->k_free[ks]));
             ++kn;
           }
           for (int j = 0; j < w.n_kv && ok; ++j) {
             const bool has_next = j + 1 < w.n_kv;
+            const bool pv = j >= jlo && j < jhi;                  // P V_t(j) at this step
+            const bool s_next = j + 1 >= jlo && j + 1 < jhi;      // S_t(j + 1) at this step
             // Operands and turn first: they are normally settled long before
             // P_t(j) is, so the wait for P is the last thing before the MMAs.
             // With a one-slot K ring, K_{j+1} only starts loading once both
@@ -1099,8 +1139,8 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             }
             ok = take_turn();
             if (!ok) break;
-            if (mine) {
-              if (j == 0) {
+            if (pv) {
+              if (j == jlo) {
                 ok = wait_warp(ptx::smem_u32(&cb->o_free[t]), (ofn & 1) ^ 1, abort_flag,
                                args.status, args.wait_limit_ns);
                 ++ofn;
@@ -1110,7 +1150,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                 ok = wait_warp(ptx::smem_u32(&cb->p_half[t]), pn & 1, abort_flag, args.status, args.wait_limit_ns);
                 if (!ok) break;
                 ptx::tc_fence_after();
-                issue_pv_h(v_ring + vs * C::v_slot_bytes, j == 0, 0);
+                issue_pv_h(v_ring + vs * C::v_slot_bytes, j == jlo, 0);
               }
               ok = wait_warp(ptx::smem_u32(&cb->p_full[t]), pn & 1, abort_flag, args.status, args.wait_limit_ns);
               ++pn;
@@ -1119,23 +1159,22 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
               if (C::split_pv)
                 issue_pv_h(v_ring + vs * C::v_slot_bytes, false, 1);
               else
-                issue_pv(v_ring + vs * C::v_slot_bytes, j == 0);
+                issue_pv(v_ring + vs * C::v_slot_bytes, j == jlo);
             }
             if (!kEarlyK && has_next) {
               ok = wait_k();
               if (!ok) break;
               ptx::tc_fence_after();
             }
-            if (mine && has_next) issue_s(k_ring + ks * C::k_slot_bytes);
+            if (s_next) issue_s(k_ring + ks * C::k_slot_bytes);
             // The other issuer goes next, then the commits (a commit tracks
             // this thread's MMAs alone; issuing one costs the warp time that
             // would otherwise delay the other query tile's MMAs).
             pass_turn();
-            if (mine) {
-              ptx::mma_commit_elect(ptx::smem_u32(has_next ? &cb->s_full[t] : &cb->o_full[t]));
-              if (!C::stage_o && j + 2 == w.n_kv)
-                ptx::mma_commit_elect(ptx::smem_u32(&cb->q_free[qb]));
-            }
+            if (s_next) ptx::mma_commit_elect(ptx::smem_u32(&cb->s_full[t]));
+            if (pv && j + 1 == jhi) ptx::mma_commit_elect(ptx::smem_u32(&cb->o_full[t]));
+            if (!C::stage_o && s_next && j + 2 == jhi)
+              ptx::mma_commit_elect(ptx::smem_u32(&cb->q_free[qb]));
             if (has_next) ptx::mma_commit_elect(ptx::smem_u32(&cb->k_free[ks]));
             ptx::mma_commit_elect(ptx::smem_u32(&cb->v_free[vs]));
           }
@@ -1189,13 +1228,15 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
       // Query token of this row within the sequence.
       const int i = w.row0 + ((t * kBM + row_in_tile) >> pshift);
       const bool row_valid = i < w.lq;
+      int jlo = 0, jhi = w.n_kv;  // this tile's key tiles (its issuer walks the same)
+      if (C::tile_ranges) tile_kv_range(w, t, args.wl, args.wr, pshift, jlo, jhi);
       // Every row of the tile a token of one sequence (one head per tile):
       // the staged O rows leave with one tensor store instead of one bulk
       // copy per row (128 copies per tile queue up in the copy engine, ahead
       // of the next item's loads; 256-token ViT windows at d80: 54.0 -> 49.8
       // us).  Packs of short segments keep the per-row copies (measured:
       // the tile store made 64-token windows 8 % slower).
-      const bool whole_o = C::stage_o && w.n_kv > 0 && pshift == 0 && w.nb == 1 &&
+      const bool whole_o = C::stage_o && jhi > jlo && pshift == 0 && w.nb == 1 &&
                            w.row0 + (t + 1) * kBM <= w.lq;
       const int off = w.lk - w.lq;
       int lo_i = 0, hi_i = 0;
@@ -1219,7 +1260,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
       }
       float m_used = neg_inf;  // running max, scaled log2 units
       float l = 0.f;
-      for (int j = 0; j < w.n_kv; ++j) {
+      for (int j = jlo; j < jhi; ++j) {
         ok = wait_warp(ptx::smem_u32(&cb->s_full[t]), sn & 1, abort_flag, args.status, args.wait_limit_ns);
         ++sn;
         if (!ok) break;
@@ -1262,7 +1303,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         if (__any_sync(0xffffffffu, need)) {
           const float m_new = fmaxf(m_used, m_tile);
           const float alpha = (m_used == neg_inf) ? 0.f : ptx::ex2(m_used - m_new);
-          if (j > 0) {
+          if (j > jlo) {
             // O_t holds the sum of the earlier tiles (its PV has completed:
             // the commit that released this S tile came after it).
 #pragma unroll
@@ -1329,7 +1370,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         // Split-KV: this CTA holds one part of the item.  Its O stays in
         // TMEM for the cluster combine, and (m, l) go into the row's first
         // two S/P columns, dead once the last P V (before o_full) is done.
-        if (w.n_kv > 0) {
+        if (jhi > jlo) {
           ok = wait_warp(ptx::smem_u32(&cb->o_full[t]), on & 1, abort_flag, args.status, args.wait_limit_ns);
           ++on;
           if (!ok) break;
@@ -1343,7 +1384,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
 
       // ---- epilogue: O / l -> bf16 rows, LSE
       uint32_t o[C::pv_n];
-      if (w.n_kv > 0) {
+      if (jhi > jlo) {
         ok = wait_warp(ptx::smem_u32(&cb->o_full[t]), on & 1, abort_flag, args.status, args.wait_limit_ns);
         ++on;
         if (!ok) break;
@@ -1359,7 +1400,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
 #pragma unroll
         for (int c = 0; c < C::pv_n; ++c) o[c] = 0u;
       }
-      const bool staged = C::stage_o && w.n_kv > 0;
+      const bool staged = C::stage_o && jhi > jlo;
       // Query head of this row (packed heads: row % P).
       const int head = w.head + (row_in_tile & ((1 << pshift) - 1));
       uint8_t* const srow = q_base + qb * C::q_tile_bytes + row_in_tile * (D_V * 2);
@@ -1414,7 +1455,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           ptx::bulk_commit();
         }
       }
-      if (staged) staged_qb = qb;
+      // The Q buffer (loaded for every item with key tiles) is released once
+      // any staged rows have been read out.
+      if (C::stage_o && w.n_kv > 0) staged_qb = qb;
     }
     release_staged();
     ptx::bulk_wait_all();  // every O row written before the CTA exits
@@ -1429,7 +1472,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         ptx::tc_fence_after();
         const int r = t * kBM + row_in_tile;  // row within the item
         uint8_t* row = smem + r * SplitStash<D_V>::kRowBytes;
-        const bool has_o = w.n_kv > 0;
+        int jlo = 0, jhi = w.n_kv;
+        if (C::tile_ranges) tile_kv_range(w, t, args.wl, args.wr, pshift, jlo, jhi);
+        const bool has_o = jhi > jlo;
         float sp_m = neg_inf, sp_l = 0.f;
         if (has_o) {
           uint32_t ml[2];
