@@ -114,7 +114,9 @@ typedef enum {
  *   out           bf16 [total_q, num_heads, d_v]  (written)
  *   lse           fp32 [num_heads, total_q] natural-log LSE, or NULL.
  *
- * A query row with no visible key gets O = 0 and LSE = -inf.
+ * A query row with no visible key gets O = 0 and LSE = -inf.  With
+ * total_q = 0 nothing is launched (q, out and lse may then be NULL); with
+ * total_k = 0 every row has no visible key (k and v may then be NULL).
  *
  * Split-KV ([flash_attn] FA4SplitKVCombineKernel): when the work items
  * (query head x 256 query rows of a sequence) cannot fill half of the SMs
@@ -207,6 +209,8 @@ fa_status fa_varlen_fwd_strided(const void* q, long long q_row_stride, long long
  *   softmax_scale scale of the 576-wide dot product (> 0)
  *   out           bf16 [num_tokens, num_heads, 512]: sum_j p_j * row_j[0:512]
  *   lse           fp32 [num_heads, num_tokens] or NULL
+ *   With num_tokens = 0 nothing is launched (q, page_table, topk_idx, out
+ *   and lse may then be NULL).
  *
  * The (token, head group, 64-key tile) work is spread evenly over the SMs.
  * When a token's keys end up on several CTAs, their partial results go to a

@@ -144,6 +144,21 @@ def test_decode_host_validation(lib, kw, expect):
     assert decode(lib, **kw) == expect
 
 
+def test_empty_extents_accept_null_buffers(lib):
+    """Zero rows may come with null buffers (an empty torch tensor has no
+    storage); without a GPU the call then fails only at the device query."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert varlen(lib, q=None, out=None, total_q=0) in (fa.FA_ERR_LAUNCH, fa.FA_ERR_ARCH)
+    assert varlen(lib, k=None, v=None, total_k=0) in (fa.FA_ERR_LAUNCH, fa.FA_ERR_ARCH)
+    assert decode(lib, q=None, pt=None, ti=None, out=None, T=0) in (fa.FA_ERR_LAUNCH,
+                                                                    fa.FA_ERR_ARCH)
+    # ... but not with rows.
+    assert varlen(lib, q=None, out=None) == fa.FA_ERR_INVALID_ARG
+    assert decode(lib, q=None, T=1) == fa.FA_ERR_INVALID_ARG
+
+
 def test_valid_arguments_without_gpu_fail_cleanly(lib):
     """With no usable device the call returns a status instead of crashing."""
     import torch

@@ -141,3 +141,16 @@ def test_topk_above_one_cta_range(cuda_device, T, H, topk, context):
     a = run_gpu(q, cache, pt, ti, scale)
     b = run_gpu(q, cache, pt, ti, scale)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_zero_tokens(cuda_device):
+    dev = torch.device("cuda:0")
+    q = torch.zeros((0, 64, 576), dtype=torch.bfloat16, device=dev)
+    cache = torch.zeros((4, 64, 576), dtype=torch.bfloat16, device=dev)
+    pt = torch.zeros((0, 4), dtype=torch.int32, device=dev)
+    ti = torch.zeros((0, 128), dtype=torch.int32, device=dev)
+    out, lse = fa.fa_sparse_mla_decode(q, cache, pt, ti, 576 ** -0.5, return_lse=True)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 64, 512)
+    assert fa.fa_sparse_mla_decode_plan(0, 64, 128) == (0, 0)
+    assert fa.fa_get_device_status() == fa.FA_OK

@@ -273,3 +273,28 @@ def test_full_size_sampled_rows(cuda_device, name):
     rows = sample_rows(w.lens_q, w.num_heads, 160, seed=len(name))
     compare(q, k, v, cq, ck, w.softmax_scale, w.causal, *w.window, rows=rows, out=out, lse=lse)
     assert fa.fa_get_device_status() == fa.FA_OK
+
+
+def test_no_keys_at_all(cuda_device):
+    # total_k = 0: every row has no visible key (O = 0, LSE = -inf), with and
+    # without the causal mask.
+    lens_q, lens_k = [5, 130, 1], [0, 0, 0]
+    q, k, v, cq, ck = make(lens_q, lens_k, 2, 2, 64, 64, seed=32)
+    assert k.shape[0] == 0
+    for causal in (False, True):
+        out, lse = run_gpu(q, k, v, cq, ck, 0.125, causal=causal)
+        assert torch.all(out == 0)
+        assert torch.all(lse == -float("inf"))
+
+
+def test_all_sequences_empty(cuda_device):
+    # total_q = 0: nothing to compute, nothing written, no error.
+    q = torch.zeros((0, 2, 64), dtype=torch.bfloat16, device="cuda:0")
+    k = torch.randn((10, 2, 64), device="cuda:0").bfloat16()
+    v = torch.randn((10, 2, 64), device="cuda:0").bfloat16()
+    cq = torch.zeros(3, dtype=torch.int32, device="cuda:0")
+    ck = torch.tensor([0, 4, 10], dtype=torch.int32, device="cuda:0")
+    out, lse = fa.fa_varlen_fwd(q, k, v, cq, ck, 0, 0, 0.125, return_lse=True)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 2, 64) and lse.shape == (2, 0)
+    assert fa.fa_get_device_status() == fa.FA_OK

@@ -262,8 +262,9 @@ extern "C" fa_status fa_varlen_fwd_strided(
     int total_q, int total_k, int num_heads, int num_heads_k, int d_qk, int d_v,
     int max_seqlen_q, int max_seqlen_k, float softmax_scale, int causal, int window_left,
     int window_right, void* out, float* lse, fa_stream_t stream) {
-  // ---- host validation (before any CUDA call)
-  if (!q || !out || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
+  // ---- host validation (before any CUDA call); q and out may be null only
+  // when they have no rows
+  if ((total_q > 0 && (!q || !out)) || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
   if (total_k > 0 && (!k || !v)) return FA_ERR_INVALID_ARG;
   if (batch < 1 || total_q < 0 || total_k < 0 || num_heads < 1 || num_heads_k < 1 ||
       num_heads % num_heads_k != 0)
@@ -465,7 +466,9 @@ fa_status plan_decode(const void* q, const void* kv_cache, const int* page_table
                       const int* topk_idx, int num_tokens, int num_heads, int topk,
                       int num_pages, int max_pages_per_tok, float softmax_scale, void* out,
                       float* lse, DecodePlan* plan) {
-  if (!q || !kv_cache || !page_table || !topk_idx || !out) return FA_ERR_INVALID_ARG;
+  // q, page_table, topk_idx and out may be null only when there are no tokens.
+  if (!kv_cache || (num_tokens > 0 && (!q || !page_table || !topk_idx || !out)))
+    return FA_ERR_INVALID_ARG;
   if (num_tokens < 0 || num_pages < 1 || max_pages_per_tok < 1 || topk < 1)
     return FA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return FA_ERR_INVALID_ARG;
