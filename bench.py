@@ -50,7 +50,7 @@ L2_FLUSH_BYTES = 512 << 20
 _CSRC = os.path.join(REPO, "varlen_flashattention_forward_gb300", "csrc")
 MEASURED_TRAFFIC = {
     # profiles/varlen_fwd_long_65536_d128.md: one full-size launch
-    "long_65536": (1.18e9 + 257.80e6, "9c8cf0bc43b46d0f", ["varlen_fwd_kernel.cuh", "sm103_ptx.cuh"]),
+    "long_65536": (1.16e9 + 258.51e6, "dc63b84dc5467252", ["varlen_fwd_kernel.cuh", "sm103_ptx.cuh"]),
     # profiles/varlen_fwd_vit_full_d80.md
     "vit_full_d80": (158.57e6, "c9acca5aecc18da4", ["varlen_fwd_kernel.cuh", "sm103_ptx.cuh"]),
     # profiles/sparse_decode_128tok.md: 32-token capture scaled by tokens to 128

@@ -71,7 +71,7 @@ constexpr int kRowsPerItem = 2 * kBM; // two query tiles per work item
 constexpr int kMaxBatch = 2048;       // sequences per launch (larger batches: several launches)
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold, log2 units
 constexpr int kSmemBudget = 232448;   // 227 KB opt-in per CTA
-constexpr int kBarrierBytes = 448;    // VarlenBarriers, reserved in the smem budget
+constexpr int kBarrierBytes = 480;    // VarlenBarriers, reserved in the smem budget
 
 constexpr unsigned int kStatusTimeout = 1u;
 
@@ -162,7 +162,16 @@ struct VarlenCfg {
   // running for d_qk > d_v (MLA 192/128: long S groups, one K slot),
   // where turns cost more than they save (causal 4 x 4096: 794 vs 699
   // TFLOP/s).
-  static constexpr bool turns = D_QK == D_V;
+  // P in TMEM columns of its own, next to O_t, where d_v leaves them free
+  // (d_v <= 64: 2 x (128 S + 64 O + 64 P) = 512 columns): S_t(j + 1) is then
+  // issued as soon as the softmax has loaded S_t(j), not after it has
+  // written P_t(j), so that the tile's next S runs during its exp2 phase
+  // and the softmax of step j + 1 finds S waiting (ViT d64: 406 -> 396 us;
+  // the step is then bound by the softmax's own exp2 and TMEM latency).
+  static constexpr bool p_cols = pv_n <= 64;
+  // Not with p_cols, where the two tiles' S issues taking turns measured
+  // 7 % slower on ViT d64 (424.6 against 395.9 us free running).
+  static constexpr bool turns = D_QK == D_V && !p_cols;
   // P V is issued in two halves of 64 keys: the softmax hands over the
   // first half of P before it computes the second, so that half of P V runs
   // while the softmax is still busy (it shortens each tile's chain softmax ->
@@ -178,6 +187,10 @@ struct VarlenCfg {
   // TMEM columns of the S/P and O regions of query tile t.
   __host__ __device__ static constexpr uint32_t s_col(int t) { return 128u * (uint32_t)t; }
   __host__ __device__ static constexpr uint32_t o_col(int t) { return 256u + 128u * (uint32_t)t; }
+  // P_t (bf16 pairs, 64 columns): its own columns with p_cols, else S_t's.
+  __host__ __device__ static constexpr uint32_t p_col(int t) {
+    return p_cols ? o_col(t) + 64u : s_col(t);
+  }
 };
 
 struct VarlenArgs {
@@ -225,6 +238,8 @@ struct alignas(8) VarlenBarriers {
   uint64_t o_free[2];
   uint64_t drain;
   uint64_t turn[2];  // issuer t may issue its next group
+  uint64_t s_free[2];   // p_cols: the softmax has loaded S_t(j)
+  uint64_t pv_done[2];  // p_cols: P V_t(j) completed (not the tile's last)
   uint64_t k_full[8];   // K ring slot landed
   uint64_t k_free[8];   // K ring slot released (one arrival per issuer)
   uint64_t v_full[8];
@@ -842,6 +857,8 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
       ptx::mbar_init(ptx::smem_u32(&cb->p_half[t]), kBM);
       ptx::mbar_init(ptx::smem_u32(&cb->o_full[t]), 1);
       ptx::mbar_init(ptx::smem_u32(&cb->o_free[t]), kBM);
+      ptx::mbar_init(ptx::smem_u32(&cb->s_free[t]), kBM);
+      ptx::mbar_init(ptx::smem_u32(&cb->pv_done[t]), 1);
     }
     ptx::mbar_init(ptx::smem_u32(&cb->drain), 2);
     ptx::mbar_init(ptx::smem_u32(&cb->turn[0]), 1);
@@ -1006,6 +1023,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         uint32_t q_par = 0;   // bit b: parity of the q_full[b] phases consumed
         uint32_t item_n = 0;  // items with KV tiles so far (selects the Q pair)
         uint32_t pn = 0, ofn = 0;
+        uint32_t sfn = 0;     // s_free phases consumed (p_cols)
         uint32_t groups = 0;  // issue groups done by this issuer
         // Wait for this issuer's turn; issuer 0 starts.
         auto take_turn = [&]() -> bool {
@@ -1048,7 +1066,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           const uint64_t vd = ptx::smem_desc(ptx::smem_u32(vbuf), C::v_atom_bytes, 8 * kRowBytes,
                                              layout_for_width(C::v_atom));
           // 16 keys = 16 rows of kRowBytes: kRowBytes 16-byte units per step.
-          issue_pv_group<kRowBytes>(tmem + C::o_col(t), tmem + C::s_col(t), vd, idesc_pv,
+          issue_pv_group<kRowBytes>(tmem + C::o_col(t), tmem + C::p_col(t), vd, idesc_pv,
                                     first ? 0u : 1u);
         };
         auto issue_pv_h = [&](const uint8_t* vbuf, bool first, int h) {
@@ -1056,7 +1074,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           constexpr uint32_t kRowBytes = C::v_atom * 2;
           const uint64_t vd = ptx::smem_desc(ptx::smem_u32(vbuf), C::v_atom_bytes, 8 * kRowBytes,
                                              layout_for_width(C::v_atom));
-          issue_pv_half<kRowBytes>(tmem + C::o_col(t), tmem + C::s_col(t), vd, idesc_pv,
+          issue_pv_half<kRowBytes>(tmem + C::o_col(t), tmem + C::p_col(t), vd, idesc_pv,
                                    first ? 0u : 1u, h);
         };
         // Both issuers walk every KV tile of every item (to stay in phase on
@@ -1112,71 +1130,138 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             ptx::mma_commit_elect(ptx::smem_u32(&cb->k_free[ks]));
             ++kn;
           }
-          for (int j = 0; j < w.n_kv && ok; ++j) {
-            const bool has_next = j + 1 < w.n_kv;
-            const bool pv = j >= jlo && j < jhi;                  // P V_t(j) at this step
-            const bool s_next = j + 1 >= jlo && j + 1 < jhi;      // S_t(j + 1) at this step
-            // Operands and turn first: they are normally settled long before
-            // P_t(j) is, so the wait for P is the last thing before the MMAs.
-            // With a one-slot K ring, K_{j+1} only starts loading once both
-            // tiles' S(j) are done, so it is waited for after P V_j instead.
-            constexpr bool kEarlyK = NK > 1;
-            const uint32_t vs = ring_slot<NV>(vn);
-            ok = wait_warp(ptx::smem_u32(&cb->v_full[vs]), (vn / NV) & 1, abort_flag,
-                           args.status, args.wait_limit_ns);
-            if (!ok) break;
-            ++vn;
-            const uint32_t ks = ring_slot<NK>(kn);
-            auto wait_k = [&]() -> bool {
-              const bool r = wait_warp(ptx::smem_u32(&cb->k_full[ks]), (kn / NK) & 1, abort_flag,
-                                       args.status, args.wait_limit_ns);
-              ++kn;
-              return r;
-            };
-            if (kEarlyK && has_next) {
-              ok = wait_k();
-              if (!ok) break;
-            }
-            ok = take_turn();
-            if (!ok) break;
-            if (pv) {
-              if (j == jlo) {
-                ok = wait_warp(ptx::smem_u32(&cb->o_free[t]), (ofn & 1) ^ 1, abort_flag,
+          if constexpr (C::p_cols) {
+            for (int j = 0; j < w.n_kv && ok; ++j) {
+              const bool has_next = j + 1 < w.n_kv;
+              const bool pv = j >= jlo && j < jhi;              // P V_t(j) at this step
+              const bool s_next = j + 1 >= jlo && j + 1 < jhi;  // S_t(j + 1) at this step
+              // S_t(j + 1) once K_{j+1} has landed and the softmax has
+              // loaded S_t(j) out of the columns it overwrites.
+              if (has_next) {
+                const uint32_t ks = ring_slot<NK>(kn);
+                ok = wait_warp(ptx::smem_u32(&cb->k_full[ks]), (kn / NK) & 1, abort_flag,
                                args.status, args.wait_limit_ns);
-                ++ofn;
+                ++kn;
                 if (!ok) break;
+                if (pv && s_next) {
+                  ok = wait_warp(ptx::smem_u32(&cb->s_free[t]), sfn & 1, abort_flag, args.status,
+                                 args.wait_limit_ns);
+                  ++sfn;
+                  if (!ok) break;
+                }
+                ptx::tc_fence_after();
+                if (s_next) {
+                  issue_s(k_ring + ks * C::k_slot_bytes);
+                  ptx::mma_commit_elect(ptx::smem_u32(&cb->s_full[t]));
+                  if (!C::stage_o && j + 2 == jhi)
+                    ptx::mma_commit_elect(ptx::smem_u32(&cb->q_free[qb]));
+                }
+                ptx::mma_commit_elect(ptx::smem_u32(&cb->k_free[ks]));
               }
-              if (C::split_pv) {
-                ok = wait_warp(ptx::smem_u32(&cb->p_half[t]), pn & 1, abort_flag, args.status, args.wait_limit_ns);
+              // P V_t(j) once V_j has landed and the softmax has written
+              // P_t(j) (keys 0..63 first with split_pv).
+              const uint32_t vs = ring_slot<NV>(vn);
+              ok = wait_warp(ptx::smem_u32(&cb->v_full[vs]), (vn / NV) & 1, abort_flag,
+                             args.status, args.wait_limit_ns);
+              ++vn;
+              if (!ok) break;
+              if (pv) {
+                if (j == jlo) {
+                  ok = wait_warp(ptx::smem_u32(&cb->o_free[t]), (ofn & 1) ^ 1, abort_flag,
+                                 args.status, args.wait_limit_ns);
+                  ++ofn;
+                  if (!ok) break;
+                }
+                if (C::split_pv) {
+                  ok = wait_warp(ptx::smem_u32(&cb->p_half[t]), pn & 1, abort_flag, args.status,
+                                 args.wait_limit_ns);
+                  if (!ok) break;
+                  ptx::tc_fence_after();
+                  issue_pv_h(v_ring + vs * C::v_slot_bytes, j == jlo, 0);
+                }
+                ok = wait_warp(ptx::smem_u32(&cb->p_full[t]), pn & 1, abort_flag, args.status,
+                               args.wait_limit_ns);
+                ++pn;
                 if (!ok) break;
                 ptx::tc_fence_after();
-                issue_pv_h(v_ring + vs * C::v_slot_bytes, j == jlo, 0);
+                if (C::split_pv)
+                  issue_pv_h(v_ring + vs * C::v_slot_bytes, false, 1);
+                else
+                  issue_pv(v_ring + vs * C::v_slot_bytes, j == jlo);
+                // The softmax of step j + 1 rescales O_t and overwrites P_t
+                // only after this P V; the tile's last one ends in o_full.
+                ptx::mma_commit_elect(
+                    ptx::smem_u32(j + 1 == jhi ? &cb->o_full[t] : &cb->pv_done[t]));
               }
-              ok = wait_warp(ptx::smem_u32(&cb->p_full[t]), pn & 1, abort_flag, args.status, args.wait_limit_ns);
-              ++pn;
-              if (!ok) break;
-              ptx::tc_fence_after();
-              if (C::split_pv)
-                issue_pv_h(v_ring + vs * C::v_slot_bytes, false, 1);
-              else
-                issue_pv(v_ring + vs * C::v_slot_bytes, j == jlo);
+              ptx::mma_commit_elect(ptx::smem_u32(&cb->v_free[vs]));
             }
-            if (!kEarlyK && has_next) {
-              ok = wait_k();
+          } else {
+            for (int j = 0; j < w.n_kv && ok; ++j) {
+              const bool has_next = j + 1 < w.n_kv;
+              const bool pv = j >= jlo && j < jhi;                  // P V_t(j) at this step
+              const bool s_next = j + 1 >= jlo && j + 1 < jhi;      // S_t(j + 1) at this step
+              // Operands and turn first: they are normally settled long before
+              // P_t(j) is, so the wait for P is the last thing before the MMAs.
+              // With a one-slot K ring, K_{j+1} only starts loading once both
+              // tiles' S(j) are done, so it is waited for after P V_j instead.
+              constexpr bool kEarlyK = NK > 1;
+              const uint32_t vs = ring_slot<NV>(vn);
+              ok = wait_warp(ptx::smem_u32(&cb->v_full[vs]), (vn / NV) & 1, abort_flag,
+                             args.status, args.wait_limit_ns);
               if (!ok) break;
-              ptx::tc_fence_after();
+              ++vn;
+              const uint32_t ks = ring_slot<NK>(kn);
+              auto wait_k = [&]() -> bool {
+                const bool r = wait_warp(ptx::smem_u32(&cb->k_full[ks]), (kn / NK) & 1, abort_flag,
+                                         args.status, args.wait_limit_ns);
+                ++kn;
+                return r;
+              };
+              if (kEarlyK && has_next) {
+                ok = wait_k();
+                if (!ok) break;
+              }
+              ok = take_turn();
+              if (!ok) break;
+              if (pv) {
+                if (j == jlo) {
+                  ok = wait_warp(ptx::smem_u32(&cb->o_free[t]), (ofn & 1) ^ 1, abort_flag,
+                                 args.status, args.wait_limit_ns);
+                  ++ofn;
+                  if (!ok) break;
+                }
+                if (C::split_pv) {
+                  ok = wait_warp(ptx::smem_u32(&cb->p_half[t]), pn & 1, abort_flag, args.status, args.wait_limit_ns);
+                  if (!ok) break;
+                  ptx::tc_fence_after();
+                  issue_pv_h(v_ring + vs * C::v_slot_bytes, j == jlo, 0);
+                }
+                ok = wait_warp(ptx::smem_u32(&cb->p_full[t]), pn & 1, abort_flag, args.status, args.wait_limit_ns);
+                ++pn;
+                if (!ok) break;
+                ptx::tc_fence_after();
+                if (C::split_pv)
+                  issue_pv_h(v_ring + vs * C::v_slot_bytes, false, 1);
+                else
+                  issue_pv(v_ring + vs * C::v_slot_bytes, j == jlo);
+              }
+              if (!kEarlyK && has_next) {
+                ok = wait_k();
+                if (!ok) break;
+                ptx::tc_fence_after();
+              }
+              if (s_next) issue_s(k_ring + ks * C::k_slot_bytes);
+              // The other issuer goes next, then the commits (a commit tracks
+              // this thread's MMAs alone; issuing one costs the warp time that
+              // would otherwise delay the other query tile's MMAs).
+              pass_turn();
+              if (s_next) ptx::mma_commit_elect(ptx::smem_u32(&cb->s_full[t]));
+              if (pv && j + 1 == jhi) ptx::mma_commit_elect(ptx::smem_u32(&cb->o_full[t]));
+              if (!C::stage_o && s_next && j + 2 == jhi)
+                ptx::mma_commit_elect(ptx::smem_u32(&cb->q_free[qb]));
+              if (has_next) ptx::mma_commit_elect(ptx::smem_u32(&cb->k_free[ks]));
+              ptx::mma_commit_elect(ptx::smem_u32(&cb->v_free[vs]));
             }
-            if (s_next) issue_s(k_ring + ks * C::k_slot_bytes);
-            // The other issuer goes next, then the commits (a commit tracks
-            // this thread's MMAs alone; issuing one costs the warp time that
-            // would otherwise delay the other query tile's MMAs).
-            pass_turn();
-            if (s_next) ptx::mma_commit_elect(ptx::smem_u32(&cb->s_full[t]));
-            if (pv && j + 1 == jhi) ptx::mma_commit_elect(ptx::smem_u32(&cb->o_full[t]));
-            if (!C::stage_o && s_next && j + 2 == jhi)
-              ptx::mma_commit_elect(ptx::smem_u32(&cb->q_free[qb]));
-            if (has_next) ptx::mma_commit_elect(ptx::smem_u32(&cb->k_free[ks]));
-            ptx::mma_commit_elect(ptx::smem_u32(&cb->v_free[vs]));
           }
         }
         // Drain: every MMA issued by either issuer completes before TMEM is
@@ -1193,9 +1278,11 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t s_addr = tmem + lane_base + C::s_col(t);
     const uint32_t o_addr = tmem + lane_base + C::o_col(t);
+    const uint32_t p_addr = tmem + lane_base + C::p_col(t);
     const float sl2 = args.scale_log2;
     const float neg_inf = -__int_as_float(0x7f800000);
     uint32_t sn = 0, on = 0;
+    uint32_t pdn = 0;     // pv_done phases consumed (p_cols)
     uint32_t item_n = 0;  // items with KV tiles so far (selects the Q pair)
     int staged_qb = -1;   // Q buffer holding O rows still being copied out
     // Releases the Q buffer of the last staged O once its copies have read it.
@@ -1275,6 +1362,11 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         for (int q = 0; q < kBN / 16; ++q) ptx::reg_fence16f(s + q * 16);
 #pragma unroll
         for (int q = 0; q < kBN / 32; ++q) ptx::reg_fence1f(qmax[q]);
+        if (C::p_cols && j + 1 < jhi) {
+          // S_t(j) is in registers: its columns may take S_t(j + 1).
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(ptx::smem_u32(&cb->s_free[t]));
+        }
 
         const int k0 = (w.tile_lo + j) * kBN;
         float row_max;
@@ -1300,22 +1392,34 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         }
         const float m_tile = row_max * sl2;  // -inf stays -inf
         const bool need = m_tile > m_used + kRescaleLog2;
+        // O_t *= alpha for a rescale (the running max moved by more than the
+        // threshold).  O_t must hold the sum of the earlier tiles: their P V
+        // has completed (the commit that released this S tile came after
+        // it; with p_cols, the pv_done wait before the call).
+        auto rescale_o = [&](float alpha) {
+#pragma unroll
+          for (int c0 = 0; c0 < C::pv_n; c0 += 16) {
+            uint32_t o[16];
+            ptx::tmem_ld16(o_addr + c0, o);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence16(o);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            ptx::tmem_st16(o_addr + c0, o);
+          }
+        };
+        // With p_cols, P V_t(j - 1) may still be running: the wait for it
+        // (and the O rescale) comes after the first half of the exp2s.
+        bool rescale_late = false;
+        float alpha_late = 1.f;
         if (__any_sync(0xffffffffu, need)) {
           const float m_new = fmaxf(m_used, m_tile);
           const float alpha = (m_used == neg_inf) ? 0.f : ptx::ex2(m_used - m_new);
-          if (j > jlo) {
-            // O_t holds the sum of the earlier tiles (its PV has completed:
-            // the commit that released this S tile came after it).
-#pragma unroll
-            for (int c0 = 0; c0 < C::pv_n; c0 += 16) {
-              uint32_t o[16];
-              ptx::tmem_ld16(o_addr + c0, o);
-              ptx::tmem_wait_ld();
-              ptx::reg_fence16(o);
-#pragma unroll
-              for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-              ptx::tmem_st16(o_addr + c0, o);
-            }
+          if (C::p_cols) {
+            rescale_late = j > jlo;
+            alpha_late = alpha;
+          } else if (j > jlo) {
+            rescale_o(alpha);
           }
           if (m_new != neg_inf) {
             l *= alpha;
@@ -1345,9 +1449,18 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             }
           };
           exp_half(IntTag<0>{});
+          if (C::p_cols && j > jlo) {
+            // P V_t(j - 1) has read P_t and added into O_t.
+            if (!wait_warp(ptx::smem_u32(&cb->pv_done[t]), pdn & 1, abort_flag, args.status,
+                           args.wait_limit_ns))
+              ok = false;
+            ++pdn;
+            ptx::tc_fence_after();
+            if (ok && rescale_late) rescale_o(alpha_late);
+          }
           if (C::split_pv) {
             // The first 64 keys' P goes out before the rest is computed.
-            ptx::tmem_st32(s_addr, pr);
+            ptx::tmem_st32(p_addr, pr);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(ptx::smem_u32(&cb->p_half[t]));
@@ -1358,8 +1471,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
           ptx::f2_unpack(ptx::add2(ls2[2], ls2[3]), b0, b1);
           l += (a0 + b0) + (a1 + b1);
         }
+        if (!ok) break;
 #pragma unroll
-        for (int q = C::split_pv ? 32 : 0; q < kBN / 2; q += 32) ptx::tmem_st32(s_addr + q, pr + q);
+        for (int q = C::split_pv ? 32 : 0; q < kBN / 2; q += 32) ptx::tmem_st32(p_addr + q, pr + q);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(ptx::smem_u32(&cb->p_full[t]));
