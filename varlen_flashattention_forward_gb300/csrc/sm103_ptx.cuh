@@ -84,6 +84,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
+// Brings the box of a 3D tensor map at {c0, c1, c2} into L2 without writing
+// shared memory (a hint: no barrier, nothing to wait for; coordinates
+// outside the tensor fetch nothing there).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int32_t c0, int32_t c1,
+                                                   int32_t c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 // 16-byte global -> shared copy, L2 only (bypasses L1).
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {

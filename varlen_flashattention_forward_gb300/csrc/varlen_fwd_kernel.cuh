@@ -155,6 +155,13 @@ struct VarlenCfg {
   static constexpr int nv = min_(8, nk + ((ring_bytes(q_pairs) - nk * (k_slot_bytes + v_slot_bytes)) /
                                           v_slot_bytes > 0 ? 1 : 0));
   static_assert(nk >= 1 && nv >= 2, "shared memory too small for the K and V rings");
+  // L2 prefetches by the producer.  With one K slot (MLA), K_{j+1} of an
+  // item as K_j goes out (causal 4 x 4096: 1979 -> 1927 us); with one Q
+  // pair and a deeper K ring (d96, d128), an item's Q and first K/V tiles
+  // when it is published (256-token windows at d128: 64-66 us against
+  // 66-68; for MLA the same prefetch cost back the gain of the K one).
+  static constexpr bool k_prefetch = nk == 1;
+  static constexpr bool item_prefetch = q_pairs == 1 && nk > 1;
   static_assert(pv_n <= 128, "O accumulator wider than its TMEM region");
   // Issue order between the two query tiles' MMA groups.  Strict turns
   // (ping-pong) for d_qk == d_v, where a group is short and free-running
@@ -942,6 +949,26 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             ptx::mbar_arrive(ptx::smem_u32(&ring->full[sl]));
           }
           if (w.n_kv == 0) continue;
+          if (C::item_prefetch) {
+            // One Q buffer pair: this item's Q and first K/V tiles load only
+            // once the previous item's last S is done.  Fetch them into L2
+            // while that item finishes, so that those loads come from there.
+            for (int t = 0; t < w.n_qt; ++t) {
+              const int row = w.q_start + w.row0 + t * (kBM >> pshift);
+#pragma unroll
+              for (int c = 0; c < QK::chunks; ++c)
+                ptx::tma_prefetch_l2_3d(c < QK::full ? &maps.q_full : &maps.q_tail, c * 64,
+                                        w.head, row);
+            }
+            const int krow = w.k_start + w.tile_lo * kBN;
+#pragma unroll
+            for (int c = 0; c < QK::chunks; ++c)
+              ptx::tma_prefetch_l2_3d(c < QK::full ? &maps.k_full : &maps.k_tail, c * 64,
+                                      w.kv_head, krow);
+#pragma unroll
+            for (int c = 0; c < C::v_atoms; ++c)
+              ptx::tma_prefetch_l2_3d(&maps.v_full, c * C::v_atom, w.kv_head, krow);
+          }
           const int pair = C::q_pairs == 2 ? (int)(item_n & 1) : 0;
           ++item_n;
           for (int t = 0; t < w.n_qt && ok; ++t) {
@@ -978,6 +1005,15 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                 ptx::tma_load_3d(ptx::smem_u32(dst + QK::chunk_off(c, kBN)),
                                  c < QK::full ? &maps.k_full : &maps.k_tail, bar, c * 64,
                                  w.kv_head, krow);
+              // With one K slot, K_{j+1} can only start loading once both
+              // tiles' S_j are done, and the MMAs wait for it: fetch it into
+              // L2 now, so that its load then comes from there.
+              if (C::k_prefetch && j + 1 < w.n_kv) {
+#pragma unroll
+                for (int c = 0; c < QK::chunks; ++c)
+                  ptx::tma_prefetch_l2_3d(c < QK::full ? &maps.k_full : &maps.k_tail, c * 64,
+                                          w.kv_head, krow + kBN);
+              }
               ++kn;
             }
             // V_j into the V ring.
