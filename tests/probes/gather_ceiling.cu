@@ -3,10 +3,11 @@
 // Each CTA stands for one decode token: it copies the 2048 rows (576 bf16,
 // 1152 bytes each) that the token's top-k selects out of a paged latent cache
 // into the same two-stage ring the decode kernel uses -- 64-row tiles of nine
-// 64-column chunks (128-byte swizzle), 128 gather threads issuing 16-byte
+// 64-column chunks (128-byte swizzle), gather threads issuing 16-byte
 // cp.async with an evict-first policy, one full barrier per chunk and one free
 // barrier per release group of chunks -- while one consumer warp releases each
-// group as soon as its chunks have landed (no MMA, no softmax).  The rows of a
+// group as soon as its chunks have landed (no MMA, no softmax).  The kernel
+// gathers with 128 threads; 192 and 256 show what more threads would give.  The rows of a
 // CTA are 2048 distinct positions of a 32768-position context laid out on
 // 64-row pages drawn from a seeded permutation of 65536 pages (4.8 GB), as in
 // the decode workload.  The time of a launch is therefore the most the decode
@@ -189,6 +190,7 @@ int main() {
   };
   for (int ctas : {128, nsm}) {
     if (run(gather_ring<128>, 128, ctas)) return 1;
+    if (run(gather_ring<192>, 192, ctas)) return 1;
     if (run(gather_ring<256>, 256, ctas)) return 1;
   }
   return failures ? 2 : 0;
