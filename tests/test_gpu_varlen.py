@@ -116,11 +116,13 @@ def test_gqa(cuda_device):
     compare(q, k, v, cq, ck, 128 ** -0.5, causal=True)
 
 
-def test_large_scores_need_rescale(cuda_device):
+@pytest.mark.parametrize("dqk,dv", [(64, 64), (80, 80), (128, 128), (192, 128)])
+def test_large_scores_need_rescale(cuda_device, dqk, dv):
     """Score ranges far beyond the lazy-rescale threshold, growing along the
-    key axis so the running max moves many times."""
+    key axis so the running max moves many times (d64 rescales O after the
+    first half of its exponentials, the other head dims before them)."""
     lens = [1000, 600]
-    q, k, v, cq, ck = make(lens, lens, 2, 2, 64, 64, seed=12, std=3.0)
+    q, k, v, cq, ck = make(lens, lens, 2, 2, dqk, dv, seed=12, std=3.0)
     ramp = torch.linspace(0.2, 3.0, k.shape[0])[:, None, None]
     k = (k.float() * ramp).bfloat16()
     compare(q, k, v, cq, ck, 0.5)
