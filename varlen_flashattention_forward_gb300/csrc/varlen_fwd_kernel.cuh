@@ -156,7 +156,11 @@ struct VarlenCfg {
                                           v_slot_bytes > 0 ? 1 : 0));
   static_assert(nk >= 1 && nv >= 2, "shared memory too small for the K and V rings");
   // L2 prefetches by the producer.  With one K slot (MLA), K_{j+1} of an
-  // item as K_j goes out (causal 4 x 4096: 1979 -> 1927 us); with one Q
+  // item as K_j goes out (causal 4 x 4096: 1979 -> 1927 us); in a split-KV
+  // launch, K_{j+1} and V_{j+1} as K_j goes out (each part streams keys no
+  // other CTA reads, and the two-slot rings of d128 keep too few bytes in
+  // flight: 256 rows x 65536 keys 154 -> 140 us; where tiles are shared
+  // between items the same prefetch cost 2-4 %); with one Q
   // pair and a deeper K ring (d96, d128), an item's Q and first K/V tiles
   // when it is published (256-token windows at d128: 64-66 us against
   // 66-68; for MLA the same prefetch cost back the gain of the K one).
@@ -1015,6 +1019,16 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                                           w.kv_head, krow + kBN);
               }
               ++kn;
+            }
+            if (kGeneral && split > 1 && j + 1 < w.n_kv) {
+              const int prow = krow + kBN;
+#pragma unroll
+              for (int c = 0; c < QK::chunks; ++c)
+                ptx::tma_prefetch_l2_3d(c < QK::full ? &maps.k_full : &maps.k_tail, c * 64,
+                                        w.kv_head, prow);
+#pragma unroll
+              for (int c = 0; c < C::v_atoms; ++c)
+                ptx::tma_prefetch_l2_3d(&maps.v_full, c * C::v_atom, w.kv_head, prow);
             }
             // V_j into the V ring.
             const uint32_t vs = ring_slot<NV>(vn);
