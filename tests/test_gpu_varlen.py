@@ -184,6 +184,40 @@ def test_strided_views(cuda_device, dqk, dv, H, Hk):
     assert torch.equal(out.cpu(), out2.cpu()) and torch.equal(lse.cpu(), lse2.cpu())
 
 
+@pytest.mark.parametrize("dqk,dv,H,Hk,lens_q,lens_k,want", [
+    # head-group packing: 4 query heads of a K/V head share a tile, the Q
+    # maps' boxes spanning heads at the strided (non-dense) head stride
+    (128, 128, 8, 2, [3, 5, 1, 17], [300, 129, 64, 500], "pack"),
+    (64, 64, 16, 1, [2, 9], [1000, 77], "pack"),
+    # split-KV over a cluster, K and V out of the combined buffer
+    (128, 128, 2, 2, [200], [20000], "split"),
+    (192, 128, 2, 2, [1, 1], [9000, 12000], "split"),
+])
+def test_strided_views_packed_and_split(cuda_device, dqk, dv, H, Hk, lens_q, lens_k, want):
+    _, split, pack = fa.fa_varlen_fwd_plan(len(lens_q), sum(lens_q), sum(lens_k), H, Hk, dqk, dv,
+                                           0, 0, True)
+    assert (pack > 1) if want == "pack" else (split > 1), (split, pack)
+    g = torch.Generator().manual_seed(18 + dqk + H)
+    Tq, Tk = sum(lens_q), sum(lens_k)
+    qbuf = torch.randn(Tq, H, dqk + 32, generator=g).bfloat16()
+    kvbuf = torch.randn(Tk, Hk, dqk + dv, generator=g).bfloat16()
+    q, k, v = qbuf[:, :, :dqk], kvbuf[:, :, :dqk], kvbuf[:, :, dqk:]
+    cq, ck = cu(lens_q), cu(lens_k)
+    dev = torch.device("cuda:0")
+    qd, kvd = qbuf.to(dev), kvbuf.to(dev)
+    out, lse = fa.fa_varlen_fwd(qd[:, :, :dqk], kvd[:, :, :dqk], kvd[:, :, dqk:], cq.to(dev),
+                                ck.to(dev), 0, 0, dqk ** -0.5, True, return_lse=True)
+    torch.cuda.synchronize()
+    compare(q.contiguous(), k.contiguous(), v.contiguous(), cq, ck, dqk ** -0.5, causal=True,
+            out=out.cpu(), lse=lse.cpu())
+    out2, lse2 = fa.fa_varlen_fwd(qd[:, :, :dqk].contiguous(), kvd[:, :, :dqk].contiguous(),
+                                  kvd[:, :, dqk:].contiguous(), cq.to(dev), ck.to(dev), 0, 0,
+                                  dqk ** -0.5, True, return_lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), out2.cpu()) and torch.equal(lse.cpu(), lse2.cpu())
+    assert fa.fa_get_device_status() == fa.FA_OK
+
+
 def test_short_segments_packed(cuda_device):
     # Runs of short segments (<= 64 rows, same token offsets in q and k) share
     # work units under a block-diagonal mask; the mix also has a long segment
