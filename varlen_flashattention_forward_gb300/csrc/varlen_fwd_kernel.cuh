@@ -6,7 +6,8 @@
 //
 //   producer warp   TMA: Q tiles once, then K_j and V_j tiles into two rings
 //                   of shared-memory slots (K ring, V ring) guarded by
-//                   mbarriers.
+//                   mbarriers; L2 prefetches where a ring is shallow (one K
+//                   slot, one Q pair, split-KV streams).
 //   MMA warps 9/10  one warp per query tile t, running converged; an
 //                   elect.sync-chosen lane issues its tcgen05.mma groups:
 //                     S_t = Q_t K_jᵀ          (SS form, fp32 accumulator in TMEM)
@@ -18,18 +19,22 @@
 //                   g, tile 1 group g, tile 0 group g+1, ...) so the tensor
 //                   core alternates between the tiles and each tile's softmax
 //                   runs while the other tile's MMAs execute (ping-pong);
-//                   for MLA shapes they run free (VarlenCfg::turns).
+//                   for MLA shapes and d_v <= 64 they run free
+//                   (VarlenCfg::turns).
 //   softmax WG t    one thread per query row (TMEM lane): loads S_t with the
 //                   sm_103 reducing TMEM load (values + per-32-column max),
 //                   masks only boundary tiles (software 3-input max there),
 //                   exp2, lazy O rescale (threshold kRescaleLog2), writes P_t
-//                   as bf16 into the S_t columns (in two halves for small
-//                   d_v, VarlenCfg::split_pv), and at the end normalises O_t
+//                   as bf16 into the S_t columns, or at d_v <= 64 into
+//                   columns of its own so that S_t(j + 1) can be issued once
+//                   S_t(j) is loaded (VarlenCfg::p_cols), in two halves for
+//                   small d_v (VarlenCfg::split_pv), and at the end normalises O_t
 //                   and writes O (through the dead Q tile and bulk copies
 //                   where VarlenCfg::stage_o) and the LSE.
 //
 // TMEM (512 columns x 128 lanes x 32 bit):
 //   [  0,128) S_0 / P_0   [128,256) S_1 / P_1   [256,384) O_0   [384,512) O_1
+//   (d_v <= 64: P_t at [320 + 128 t, +64), beside O_t)
 //
 // Shared memory: one or two pairs of Q tiles, the K ring, the V ring,
 // mbarriers, and the work list.  Q and K tiles are column chunks of
