@@ -85,7 +85,11 @@ typedef enum {
  *   v             bf16 [total_k, num_heads_k, d_v]
  *   cu_seqlens_q  int32 [batch + 1] device, non-decreasing, cu[0] = 0,
  *                 cu[batch] = total_q.  Sequence b owns query tokens
- *                 [cu_seqlens_q[b], cu_seqlens_q[b+1]).
+ *                 [cu_seqlens_q[b], cu_seqlens_q[b+1]).  The kernel
+ *                 clamps each entry to [0, total_q] and each end to at least
+ *                 its start, so a malformed array gives empty or shortened
+ *                 sequences and no access outside the tensors (rows that
+ *                 two such sequences share get either's values).
  *   cu_seqlens_k  int32 [batch + 1] device, same for keys/values.
  *   batch         >= 1.  Up to 2048 sequences run as one launch (the
  *                 kernel sorts their work list in shared memory); a larger

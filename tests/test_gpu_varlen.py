@@ -334,3 +334,56 @@ def test_all_sequences_empty(cuda_device):
     torch.cuda.synchronize()
     assert out.shape == (0, 2, 64) and lse.shape == (2, 0)
     assert fa.fa_get_device_status() == fa.FA_OK
+
+
+def _guarded(T, H, d, guard_rows, dev):
+    """out [T, H, d] and lse [H, T] as views at the start of NaN-filled
+    buffers with guard_rows more rows (resp. guard_rows * H more values)."""
+    ob = torch.full(((T + guard_rows) * H * d,), float("nan"), dtype=torch.bfloat16, device=dev)
+    lb = torch.full((H * (T + guard_rows),), float("nan"), dtype=torch.float32, device=dev)
+    return ob, lb, ob[:T * H * d].view(T, H, d), lb[:H * T].view(H, T)
+
+
+def test_cu_seqlens_past_the_tensors_are_clamped(cuda_device):
+    # The last entries point 100 tokens past total_q / total_k: the call
+    # behaves as if they ended at the tensors' ends, and writes nothing past
+    # out or lse.
+    T, H, d = 200, 2, 64
+    q, k, v, cq, ck = make([100, 100], [100, 100], H, H, d, d, seed=33)
+    bad = torch.tensor([0, 100, 300], dtype=torch.int32)
+    dev = torch.device("cuda:0")
+    ob, lb, out, lse = _guarded(T, H, d, 64, dev)
+    fa.fa_varlen_fwd(q.to(dev), k.to(dev), v.to(dev), bad.to(dev), bad.to(dev), 0, 0, 0.125,
+                     True, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.isnan(ob[T * H * d:].float()).all() and torch.isnan(lb[H * T:]).all()
+    compare(q, k, v, cq, ck, 0.125, causal=True, out=out.cpu(), lse=lse.cpu())
+    assert fa.fa_get_device_status() == fa.FA_OK
+
+
+def test_decreasing_cu_seqlens_give_empty_sequences(cuda_device):
+    # cu = [0, 100, 60, 200]: sequence 1 would end before it starts (empty),
+    # sequence 2 covers tokens [60, 200) and overlaps sequence 0's last 40
+    # rows, whose values are then undefined.  The rows only one sequence
+    # writes must match that sequence alone, and nothing is written past out.
+    T, H, d = 200, 2, 64
+    g = torch.Generator().manual_seed(34)
+    q = torch.randn(T, H, d, generator=g).bfloat16()
+    k = torch.randn(T, H, d, generator=g).bfloat16()
+    v = torch.randn(T, H, d, generator=g).bfloat16()
+    bad = torch.tensor([0, 100, 60, 200], dtype=torch.int32)
+    dev = torch.device("cuda:0")
+    ob, lb, out, lse = _guarded(T, H, d, 64, dev)
+    fa.fa_varlen_fwd(q.to(dev), k.to(dev), v.to(dev), bad.to(dev), bad.to(dev), 0, 0, 0.125,
+                     False, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.isnan(ob[T * H * d:].float()).all() and torch.isnan(lb[H * T:]).all()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    out, lse = out.cpu(), lse.cpu()
+    # Sequence 0 alone owns rows [0, 60), sequence 2 alone rows [100, 200).
+    rows0 = np.arange(60 * H)
+    compare(q[:100].contiguous(), k[:100].contiguous(), v[:100].contiguous(), cu([100]),
+            cu([100]), 0.125, rows=rows0, out=out[:100], lse=lse[:, :100])
+    rows2 = np.arange(40 * H, 140 * H)
+    compare(q[60:].contiguous(), k[60:].contiguous(), v[60:].contiguous(), cu([140]), cu([140]),
+            0.125, rows=rows2, out=out[60:], lse=lse[:, 60:].contiguous())

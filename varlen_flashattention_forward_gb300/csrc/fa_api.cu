@@ -338,6 +338,7 @@ extern "C" fa_status fa_varlen_fwd_strided(
   args.num_heads = num_heads;
   args.num_heads_k = num_heads_k;
   args.total_q = total_q;
+  args.total_k = total_k;
   args.scale_log2 = softmax_scale * 1.4426950408889634f;
   args.wl = window_left;
   // Causal is the window's right edge on the bottom-right diagonal

@@ -216,6 +216,7 @@ struct VarlenArgs {
   int num_heads;
   int num_heads_k;
   int total_q;
+  int total_k;
   float scale_log2;  // softmax_scale * log2(e)
   int wl;            // window left, -1 = unbounded
   int wr;            // window right with causal folded in, -1 = unbounded
@@ -530,7 +531,19 @@ __device__ __forceinline__ bool wait_drain_warp(uint32_t bar, uint32_t parity,
 // allocation of the pipeline loops (ViT d80 1.5 % slower).
 // (The kernel arguments it needs come by value: a reference would make the
 // compiler copy the whole argument block to local memory for the call.)
+// Sequence b's token range [lo, hi) in a tensor of `total` tokens: the
+// cu_seqlens entries clamped to [0, total] and hi to at least lo, so that a
+// malformed array (decreasing, or reaching past the tensor) gives empty or
+// shortened sequences and no access outside the tensors.
+__device__ __forceinline__ int seq_lo(const int* cu, int b, int total) {
+  return min(max(__ldg(cu + b), 0), total);
+}
+__device__ __forceinline__ int seq_hi(const int* cu, int b, int total) {
+  return min(max(__ldg(cu + b + 1), seq_lo(cu, b, total)), total);
+}
+
 static __device__ __noinline__ void build_work_list(const int* cu_q, const int* cu_k, int B,
+                                                    int total_q, int total_k,
                                                     int num_heads, int pack_shift, int* s_prefix,
                                                     int* s_sorted, int* s_part, int* s_tmp) {
   const int tid = threadIdx.x;
@@ -542,8 +555,8 @@ static __device__ __noinline__ void build_work_list(const int* cu_q, const int* 
   //    packable sequence's first token (-1 for any other sequence),
   //    s_sorted[b] = its key count.
   for (int b = tid; b < B; b += kVarlenThreads) {
-    const int q0 = cu_q[b], k0 = cu_k[b];
-    const int lq = cu_q[b + 1] - q0, lk = cu_k[b + 1] - k0;
+    const int q0 = seq_lo(cu_q, b, total_q), k0 = seq_lo(cu_k, b, total_k);
+    const int lq = seq_hi(cu_q, b, total_q) - q0, lk = seq_hi(cu_k, b, total_k) - k0;
     const bool pack = pack_shift == 0 && lq >= 1 && lq <= kPackMaxLen && lk == lq && k0 == q0;
     s_prefix[b] = pack ? q0 / kPackBlock : -1;
     s_sorted[b] = lk;
@@ -667,10 +680,12 @@ __device__ __forceinline__ WorkItem decode_item(int it, const VarlenArgs& a,
   w.nb = unit >> kUnitShift;
   // Read through the read-only data cache: every role decodes every item,
   // and these few words stay cached there.
-  w.q_start = __ldg(a.cu_q + w.b0);
-  w.k_start = __ldg(a.cu_k + w.b0);
-  w.lq = __ldg(a.cu_q + w.b0 + w.nb) - w.q_start;
-  w.lk = __ldg(a.cu_k + w.b0 + w.nb) - w.k_start;
+  // (A pack's members are consecutive and contiguous, so its range runs
+  // from its first member's start to its last member's end.)
+  w.q_start = seq_lo(a.cu_q, w.b0, a.total_q);
+  w.k_start = seq_lo(a.cu_k, w.b0, a.total_k);
+  w.lq = seq_hi(a.cu_q, w.b0 + w.nb - 1, a.total_q) - w.q_start;
+  w.lk = seq_hi(a.cu_k, w.b0 + w.nb - 1, a.total_k) - w.k_start;
   // An item covers 256 / P tokens of the sequence (1 << tshift) and P heads.
   static_assert(kRowsPerItem == 256, "tokens per item are 256 >> pack_shift");
   const int tshift = 8 - pack_shift;
@@ -908,8 +923,8 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
   static_assert(SplitStash<D_V>::kBytes <= 2 * C::q_pairs * C::q_tile_bytes +
                                                NK * C::k_slot_bytes + NV * C::v_slot_bytes,
                 "the split-KV partials fit in the Q tiles and K/V rings");
-  build_work_list(args.cu_q, args.cu_k, args.batch, args.num_heads, pshift, s_prefix,
-                  s_sorted, s_part,
+  build_work_list(args.cu_q, args.cu_k, args.batch, args.total_q, args.total_k, args.num_heads,
+                  pshift, s_prefix, s_sorted, s_part,
                   reinterpret_cast<int*>(k_ring));  // ends with __syncthreads
   if (tid == 0) {
     // The decoded-item ring, in the scan scratch the list builder is done with.
@@ -1389,9 +1404,10 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         int lo = w.b0, hi = w.b0 + w.nb - 1;
         while (lo < hi) {
           const int mid = (lo + hi + 1) >> 1;
-          if (__ldg(args.cu_q + mid) <= g) lo = mid; else hi = mid - 1;
+          if (seq_lo(args.cu_q, mid, args.total_q) <= g) lo = mid; else hi = mid - 1;
         }
-        const int s0 = __ldg(args.cu_q + lo) - w.q_start, s1 = __ldg(args.cu_q + lo + 1) - w.q_start;
+        const int s0 = seq_lo(args.cu_q, lo, args.total_q) - w.q_start;
+        const int s1 = seq_hi(args.cu_q, lo, args.total_q) - w.q_start;
         lo_i = args.wl >= 0 ? max(s0, i - args.wl) : s0;
         hi_i = args.wr >= 0 ? min(s1, i + args.wr + 1) : s1;
         if (hi_i < lo_i) hi_i = lo_i;
