@@ -50,9 +50,9 @@ L2_FLUSH_BYTES = 512 << 20
 _CSRC = os.path.join(REPO, "varlen_flashattention_forward_gb300", "csrc")
 MEASURED_TRAFFIC = {
     # profiles/varlen_fwd_long_65536_d128.md: one full-size launch
-    "long_65536": (1.15e9 + 257.33e6, "82cc1a355440a909", ["varlen_fwd_kernel.cuh", "sm103_ptx.cuh"]),
+    "long_65536": (1.12e9 + 258.55e6, "5ddaada870faa9d4", ["varlen_fwd_kernel.cuh", "sm103_ptx.cuh"]),
     # profiles/varlen_fwd_vit_full_d80.md
-    "vit_full_d80": (134.28e6 + 23.82e6, "82cc1a355440a909", ["varlen_fwd_kernel.cuh", "sm103_ptx.cuh"]),
+    "vit_full_d80": (134.28e6 + 23.57e6, "5ddaada870faa9d4", ["varlen_fwd_kernel.cuh", "sm103_ptx.cuh"]),
     # profiles/sparse_decode_128tok.md: one full-size (128-token) launch
     "sparse_mla_decode": (312.92e6 + 3.65e6, "8fc87c45839316f3",
                           ["sparse_decode_kernel.cuh", "sm103_ptx.cuh", "fa_api.cu"]),
