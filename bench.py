@@ -54,7 +54,7 @@ MEASURED_TRAFFIC = {
     # profiles/varlen_fwd_vit_full_d80.md
     "vit_full_d80": (134.28e6 + 23.57e6, "5ddaada870faa9d4", ["varlen_fwd_kernel.cuh", "sm103_ptx.cuh"]),
     # profiles/sparse_decode_128tok.md: one full-size (128-token) launch
-    "sparse_mla_decode": (312.92e6 + 3.65e6, "8fc87c45839316f3",
+    "sparse_mla_decode": (312.90e6 + 3.77e6, "555aefb1cc5b44d6",
                           ["sparse_decode_kernel.cuh", "sm103_ptx.cuh", "fa_api.cu"]),
 }
 
