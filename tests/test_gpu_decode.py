@@ -66,6 +66,7 @@ def test_invalid_slots_are_skipped(cuda_device):
     ti[1, 5:40] = 1024 + 3             # past the context
     pt = pt.clone()
     pt[2, :] = -5                      # every page of token 2 out of range
+    pt[3, ::3] = cache.shape[0] + 7    # some pages of token 3 past the cache
     compare(q, cache, pt, ti, scale)
     out, lse = run_gpu(q, cache, pt, ti, scale)
     assert torch.all(out[2] == 0) and torch.all(torch.isneginf(lse[:, 2]))
