@@ -110,6 +110,16 @@ def test_sliding_windows(cuda_device, wl, wr, causal):
     compare(q, k, v, cq, ck, 128 ** -0.5, causal, wl, wr)
 
 
+@pytest.mark.parametrize("d", [64, 80])
+@pytest.mark.parametrize("wl,wr,causal", [(100, 0, True), (50, 70, False), (0, 0, False)])
+def test_sliding_windows_small_head_dims(cuda_device, d, wl, wr, causal):
+    # d64 (P in columns of its own, S issued during the softmax) and d80 (P V
+    # in two halves): window masks on boundary tiles, rows with one key.
+    lens = [700, 257, 64]
+    q, k, v, cq, ck = make(lens, lens, 2, 2, d, d, seed=40 + d + wl + wr)
+    compare(q, k, v, cq, ck, d ** -0.5, causal, wl, wr)
+
+
 def test_gqa(cuda_device):
     lens = [300, 77]
     q, k, v, cq, ck = make(lens, lens, 8, 2, 128, 128, seed=11)
